@@ -1,0 +1,317 @@
+"""Pins of the CPU oracle against facts fixed outside it.
+
+Each test ties one oracle function to something other than itself: a format
+definition's textbook values, a library routine (torch's fp8 cast, SDPA,
+scipy's logsumexp), a closed form on a hand-built cache, brute force on tiny
+inputs, or a figure the pages print (tests/golden/pages_figures.txt).
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import msa_synth as ms
+from oracle import msa_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_figures.txt")
+
+
+def golden():
+    vals = {}
+    for line in open(GOLDEN, encoding="utf-8"):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = (x.strip() for x in line.split("="))
+            vals[k] = float(v)
+    return vals
+
+
+# ---------------------------------------------------------------- formats
+
+def test_e4m3_textbook_values():
+    # OCP 8-bit floating point spec, E4M3: bias 7, max normal 448, min normal
+    # 2^-6, min subnormal 2^-9, S.1111.111 is NaN, no infinities.
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0,
+             0xB8: -1.0, 0xFE: -448.0, 0x81: -(2.0 ** -9)}
+    for code, val in table.items():
+        assert O.e4m3_value(code) == val, hex(code)
+    assert np.isnan(O.e4m3_value(0x7F)) and np.isnan(O.e4m3_value(0xFF))
+
+
+def test_e4m3_matches_torch_cast():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    mine = O.e4m3_value(codes).astype(np.float32)
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok].view(np.uint32), mine[ok].view(np.uint32))
+
+
+def test_e2m1_textbook_values():
+    # OCP MX spec, FP4 E2M1: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 = sign
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for code in range(16):
+        want = (-1.0 if code & 8 else 1.0) * mags[code & 7]
+        assert O.e2m1_value(code) == want
+
+
+def test_bf16_widen_matches_torch():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 1 << 16, size=4096, dtype=np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # drop inf/nan patterns
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(O.bf16_value(bits).view(np.uint32), ref.view(np.uint32))
+
+
+def test_nvfp4_products_exact_in_fp32():
+    # every e2m1 x e4m3 product is exact in fp32, so the dequant has one rounding
+    for n in range(16):
+        for sc in range(256):
+            if (sc & 0x7F) == 0x7F:
+                continue
+            exact = O.nvfp4_product_exact(n, sc)
+            f32 = np.float32(O.e2m1_value(n) * O.e4m3_value(sc))
+            assert exact == float(f32)
+
+
+def test_fp8_dequant_one_rounding_matches_torch():
+    rng = np.random.default_rng(1)
+    codes = rng.integers(0, 256, size=(3, 128), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    scale = rng.random(3).astype(np.float32) * 0.01
+    mine = O._dequant("fp8", codes, scale=scale)
+    ref = (torch.from_numpy(codes).view(torch.float8_e4m3fn).float()
+           * torch.from_numpy(scale)[:, None]).numpy()
+    assert np.array_equal(mine.view(np.uint32), ref.view(np.uint32))
+
+
+def test_nvfp4_roundtrip_nibble_order_and_scale_index():
+    # exactly representable input: x = e2m1 * e4m3_scale * global, with the
+    # group amax equal to 6 * scale * global so the quantizer recovers the
+    # same scale; the oracle must decode the generator's bytes back to x.
+    rng = np.random.default_rng(2)
+    gscale = 0.0078125
+    sf_codes = rng.integers(0x20, 0x60, size=(2, 8), dtype=np.uint8)
+    nib = rng.integers(0, 16, size=(2, 128), dtype=np.uint8)
+    nib[:, ::16] = 7  # magnitude 6 in every group -> amax16 = 6 * scale
+    x = O.e2m1_value(nib) * np.repeat(O.e4m3_value(sf_codes), 16, axis=-1) * gscale
+    packed, sf, g = ms.quantize_nvfp4(torch.from_numpy(x).float(), global_scale=gscale)
+    assert np.array_equal(sf.numpy(), sf_codes)
+    deq = O._dequant("nvfp4", packed.numpy(), sf=sf.numpy(), gscale=g)
+    assert np.array_equal(deq, x.astype(np.float32))
+    # element 2j is the low nibble of byte j
+    assert np.array_equal(packed.numpy()[0, 0] & 0xF, nib[0, 0] & 0xF)
+
+
+# ---------------------------------------------------------------- layout / byte figures
+
+def test_layout_bytes_match_pages():
+    g = golden()
+    w = ms.make_workload("tiny_bf16", seq_lens=(256,), kv_dtype="nvfp4", index_dtype="fp8",
+                         q_dtype="bf16")
+    c = ms.make_case(w)
+    H, D = w.num_kv_heads, w.head_dim
+    tokens = c["num_blocks"] * 128
+    nvfp4_per_elem = (c["k"].numel() + c["k_sf"].numel()) / (tokens * H * D)
+    assert nvfp4_per_elem == g["nvfp4_kv_bytes_per_token"] / g["fp8_kv_bytes_per_token"] == 9 / 16
+    assert 1 - nvfp4_per_elem == g["nvfp4_saving"]
+    # FP8 index keys: one shared head of 128 dims, 1 byte each
+    assert c["idx"].numel() / tokens == g["index_bytes_per_token_fp8"]
+    assert 2 * H * D == g["kv_bytes_per_token_fp8"]  # K + V, 4 heads x 128 dims, FP8
+    assert g["index_bytes_per_token_fp8"] / g["kv_bytes_per_token_fp8"] == g["index_to_kv_ratio"]
+    assert g["topk_blocks"] * g["block_size_tokens"] == g["max_keys_per_query"]
+
+
+def test_traffic_model_long_context_limit():
+    from block_sparse_attention_03_gb300 import roofline as R
+    g = golden()
+    dense = lambda T: g["kv_bytes_per_token_fp8"] * T
+    for T, lo, hi in [(524288, 0.128, 0.130), (1 << 30, 0.12500, 0.12501)]:
+        sparse = R.decode_bytes_per_query("fp8", "fp8", T, 16 * 128, 4, 128, 128)
+        assert lo < sparse / dense(T) < hi
+    assert abs(R.decode_bytes_per_query("fp8", "fp8", 1 << 40, 2048, 4, 128, 128) / dense(1 << 40)
+               - g["long_context_traffic_ratio"]) < 1e-6
+
+
+# ---------------------------------------------------------------- score / pool
+
+def _onehot_keys(T, Di=128):
+    keys = np.zeros((T, Di), dtype=np.float32)
+    keys[np.arange(T), np.arange(T) % Di] = 1.0
+    return keys
+
+
+def test_index_score_closed_form():
+    # key t = unit vector e_(t mod 128): score(g, t) = scale * iq[g][t mod 128]
+    T, Q, G = 300, 2, 4
+    rng = np.random.default_rng(3)
+    iq = rng.standard_normal((Q, G, 128))
+    pos = np.array([T - 2, T - 1])
+    scale = 128 ** -0.5
+    s = O.index_scores(_onehot_keys(T), iq, pos, scale)
+    for q in range(Q):
+        for g in range(G):
+            for t in range(T):
+                want = scale * iq[q, g, t % 128] if t <= pos[q] else -np.inf
+                assert s[q, g, t] == pytest.approx(want, rel=1e-14, abs=0) if t <= pos[q] else s[q, g, t] == want
+
+
+def test_pool_closed_form_with_causal_tail():
+    # key t = (1 + t // 128) * e_(t mod 128): block b's scores are (b+1) * iq
+    T, Q, G = 300, 3, 4
+    rng = np.random.default_rng(4)
+    iq = np.abs(rng.standard_normal((Q, G, 128)))
+    keys = _onehot_keys(T) * (1 + np.arange(T) // 128)[:, None]
+    pos = np.array([255, 256, 299])  # straddles the 2nd/3rd block boundary
+    s = O.index_scores(keys, iq, pos, 1.0)
+    P = O.pool_blocks(s, 4)
+    for q in range(Q):
+        for g in range(G):
+            for b in range(4):
+                n = min(128, pos[q] + 1 - b * 128, T - b * 128)
+                want = (b + 1) * iq[q, g, :n].max() if n > 0 else -np.inf
+                assert P[q, g, b] == want
+
+
+def test_scale_applies_to_scores():
+    T = 130
+    iq = np.ones((1, 1, 128))
+    s1 = O.index_scores(_onehot_keys(T), iq, np.array([T - 1]), 1.0)
+    s2 = O.index_scores(_onehot_keys(T), iq, np.array([T - 1]), 128 ** -0.5)
+    assert np.allclose(s2, s1 * 128 ** -0.5)
+
+
+# ---------------------------------------------------------------- selection
+
+def _brute_topk(pooled, recent, k):
+    """Best (k-1)-subset of the blocks before `recent` by total score."""
+    cand = list(range(recent))
+    m = min(k - 1, len(cand))
+    best = max(itertools.combinations(cand, m), key=lambda c: (sum(pooled[b] for b in c),))
+    return sorted(list(best) + [recent])
+
+
+def test_selection_matches_brute_force():
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        nb = int(rng.integers(1, 10))
+        k = int(rng.choice([2, 3, 4, 5]))
+        pooled = rng.standard_normal(nb)  # distinct values
+        pos = (nb - 1) * 128 + int(rng.integers(0, 128))
+        got = O.select_blocks(pooled, pos, k)
+        want = _brute_topk(pooled, nb - 1, k)
+        assert list(got[: len(want)]) == want
+        assert np.all(got[len(want):] == -1)
+
+
+def test_selection_ties_prefer_smaller_id():
+    pooled = np.array([1.0, 2.0, 2.0, 2.0, 0.5, 9.0])
+    got = O.select_blocks(pooled, 5 * 128 + 3, 3)  # recent = 5 forced, 2 free slots
+    assert list(got) == [1, 2, 5]
+
+
+def test_selection_invariants():
+    rng = np.random.default_rng(6)
+    for _ in range(200):
+        nb = int(rng.integers(1, 60))
+        pooled = rng.standard_normal(nb)
+        pos = (nb - 1) * 128 + int(rng.integers(0, 128))
+        for k in (4, 8, 16, 32):
+            sel = O.select_blocks(pooled, pos, k)
+            ids = sel[sel >= 0]
+            assert (nb - 1) in ids  # the most recent block is always kept
+            assert len(ids) == min(k, nb)
+            assert np.all(np.diff(ids) > 0)
+            assert len(ids) * 128 <= 2048 or k == 32  # <= 2,048 keys for k = 16
+
+
+def test_forced_init_and_local_blocks():
+    pooled = np.arange(20, dtype=float)[::-1].copy()  # block 0 best
+    sel = O.select_blocks(pooled, 19 * 128, 6, init_blocks=2, local_blocks=2)
+    assert {0, 1, 17, 18, 19}.issubset(set(sel))
+    assert len(set(sel)) == 6
+
+
+# ---------------------------------------------------------------- attend
+
+def _small_case(**kw):
+    w = ms.make_workload("tiny_bf16", **kw)
+    return w, ms.case_to_host(ms.make_case(w))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "nvfp4"])
+def test_full_topk_equals_dense_causal_sdpa(kv):
+    # top-k >= number of blocks: MSA must equal dense causal attention
+    w, c = _small_case(seq_lens=(1000, 700), q_per_seq=3, kv_dtype=kv, index_dtype=kv, topk=8)
+    r = O.run_path(c)
+    Q, G, Hq = w.q_per_seq, w.num_kv_heads, w.num_q_heads
+    for s, T in enumerate(w.seq_lens):
+        K = np.concatenate([O.dequant_kv_tile(c, "k", int(c["block_table"][s, b]))
+                            for b in range((T + 127) // 128)], axis=1)[:, :T]
+        V = np.concatenate([O.dequant_kv_tile(c, "v", int(c["block_table"][s, b]))
+                            for b in range((T + 127) // 128)], axis=1)[:, :T]
+        q = O.query_values(c["q"], w.q_dtype, c["q_scale"])[s * Q:(s + 1) * Q]
+        qt = torch.from_numpy(q).permute(1, 0, 2)[None]  # [1, Hq, Q, D]
+        kt = torch.from_numpy(K.astype(np.float64))[None]  # [1, G, T, D]
+        vt = torch.from_numpy(V.astype(np.float64))[None]
+        pos = torch.arange(T - Q, T)
+        mask = torch.arange(T)[None, :] <= pos[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, attn_mask=mask, scale=w.head_dim ** -0.5, enable_gqa=True)
+        ref = ref[0].permute(1, 0, 2).numpy()
+        assert np.allclose(r["out"][s * Q:(s + 1) * Q], ref, rtol=0, atol=1e-12)
+
+
+def test_lse_matches_scipy():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(128)
+    K = rng.standard_normal((300, 128))
+    V = rng.standard_normal((300, 128))
+    o, lse = O.attend(q, K, V, 0.1)
+    assert lse == pytest.approx(logsumexp(0.1 * K @ q), rel=1e-13)
+    w = np.exp(0.1 * K @ q - lse)
+    assert np.allclose(o, w @ V, atol=1e-12)
+
+
+def test_block_table_permutation_invariance():
+    w, c = _small_case(seq_lens=(1500,), kv_dtype="fp8", index_dtype="fp8")
+    r1 = O.run_path(c)
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(c["num_blocks"])  # new physical slot of each block
+    c2 = dict(c)
+    for key in ("idx", "idx_scale", "k", "v", "k_scale", "v_scale"):
+        arr = np.empty_like(c[key])
+        arr[perm] = c[key]
+        c2[key] = arr
+    c2["block_table"] = perm[c["block_table"]].astype(np.int32)
+    r2 = O.run_path(c2)
+    assert np.array_equal(r1["topk"], r2["topk"])
+    assert np.array_equal(r1["out"], r2["out"])
+    assert np.array_equal(r1["pooled"], r2["pooled"])
+
+
+def test_planted_hot_blocks_are_selected():
+    for kv in ("bf16", "fp8", "nvfp4"):
+        w, c = _small_case(seq_lens=(8192, 6000), kv_dtype=kv, index_dtype=kv)
+        r = O.run_path(c)
+        for s in range(w.num_seqs):
+            for g in range(w.num_kv_heads):
+                assert set(c["hot"][s, g]).issubset(set(r["topk"][s, g])), (kv, s, g)
+
+
+def test_multi_token_causal_positions():
+    # 8 verify tokens straddling a block boundary: each keeps its own block
+    w, c = _small_case(seq_lens=(128 * 6 + 3,), q_per_seq=8)
+    r = O.run_path(c)
+    T = w.seq_lens[0]
+    for i in range(8):
+        pos = T - 8 + i
+        for g in range(w.num_kv_heads):
+            assert pos // 128 in r["topk"][i, g]
+            assert np.all(np.isneginf(r["pooled"][i, g, pos // 128 + 1:]))
