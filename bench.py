@@ -1,0 +1,355 @@
+"""Benchmark of the MSA decode hot path (score -> pool -> top-k -> attend).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one msa_decode call over one batch of synthetic input (the whole
+path, every stage).  Prints ONE JSON line on rank 0.  Under torchrun with
+N > 1 every rank runs its own replica of the workload (decode batches are
+independent problems: weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA decode queries/s and HBM GB/s (% of GB300 peak), score+topk+attend"
+WORKLOAD_TEXT = {
+    "fp8_decode": "FP8 E4M3 decode: 32 seqs, context ~U[16K,32K] (seeded), 1 query token each, 16 q / 4 KV heads, "
+                  "dim 128, index dim 128, top-16 of 128-token blocks, K/V/index keys E4M3 + fp32 per-token scales, "
+                  "bf16 queries, shuffled physical block table",
+    "fp8_long": "Long-context FP8 decode: 4 seqs x 512K tokens (4096 blocks), 1 query token, 16 q / 4 KV heads, "
+                "dim 128, top-16, FP8 E4M3 K/V/index keys + per-token scales, bf16 queries",
+    "nvfp4_verify": "NVFP4 speculative verify: 8 seqs x 128K, 8 query tokens each, NVFP4 K/V/index keys, E4M3 queries",
+    "tiny_bf16": "Tiny BF16 decode: 1 seq x 4096 tokens, 1 query, BF16 everything",
+}
+KERNELS_PER_STEP = 7  # prep(index q), indexer, top-k, prep(q), union, attend, combine
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="fp8_decode", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(w, sel_union_blocks):
+    """Bytes the pages' decode model reads per step: whole-context index keys +
+    K/V of the selected blocks (union over a sequence's query tokens, per KV head)."""
+    from block_sparse_attention_03_gb300 import roofline as R
+    idx = sum(w.seq_lens) * R.index_bytes_per_token(w.index_dtype)
+    kv_tok = R.kv_bytes_per_token(w.kv_dtype, 1)  # per KV head
+    kv = 0.0
+    for s, T in enumerate(w.seq_lens):
+        for g, blocks in enumerate(sel_union_blocks[s]):
+            for b in blocks:
+                kv += min(128, T - 128 * b) * kv_tok
+    sc_idx, sc_kv = R.scale_bytes_per_token(w.kv_dtype, w.index_dtype, 1)
+    actual = idx + kv + sum(w.seq_lens) * sc_idx
+    for s, T in enumerate(w.seq_lens):
+        for blocks in sel_union_blocks[s]:
+            actual += sum(min(128, T - 128 * b) for b in blocks) * sc_kv
+    return idx, kv, actual
+
+
+def cpu_oracle_sample(w, case_host, seqs):
+    """Time the oracle (as it stands) on the whole path for the given sequences."""
+    from oracle import msa_oracle as O
+    t0 = time.perf_counter()
+    O.run_path(case_host, seqs=seqs)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on host cores, bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import msa_synth as ms
+    w = ms.make_workload(args.workload)
+    case = ms.make_case(w, device="cpu") if args.workload != "fp8_long" else None
+    if case is None:  # 512K-token contexts: generate one sequence's worth on the host
+        w = ms.make_workload(args.workload, seq_lens=(w.seq_lens[0],))
+        case = ms.make_case(w, device="cpu")
+    h = ms.case_to_host(case)
+    per_step = 1  # one sequence per step (bounded sample)
+    times = []
+    for it in range(args.warmup + args.steps):
+        s = it % w.num_seqs
+        dt = cpu_oracle_sample(w, h, [s])
+        if it >= args.warmup:
+            times.append(dt)
+    mean = sum(times) / len(times)
+    qps = per_step * w.q_per_seq / mean
+    line = {"metric": METRIC, "value": qps, "unit": "queries/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload],
+                       "sample": f"one sequence of the workload per step ({w.q_per_seq} query tokens)"},
+            "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                             "sample": "one sequence per step, whole path (score, pool, top-k, attend) in fp64"},
+            "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_attention_03_gb300 as msa
+    import msa_synth as ms
+
+    base = ms.make_workload(args.workload)
+    w = ms.make_workload(args.workload, seed=base.seed + 1000 * rank)
+    case = ms.make_case(w, device=dev)
+    cache = msa.PagedCache(kv_dtype=w.kv_dtype, index_dtype=w.index_dtype, num_blocks=case["num_blocks"],
+                           num_kv_heads=w.num_kv_heads, k=case["k"], v=case["v"], idx=case["idx"],
+                           k_sf=case.get("k_sf"), v_sf=case.get("v_sf"), k_scale=case.get("k_scale"),
+                           v_scale=case.get("v_scale"), idx_sf=case.get("idx_sf"),
+                           idx_scale=case.get("idx_scale"), k_global=case.get("k_global", 0.0),
+                           v_global=case.get("v_global", 0.0), idx_global=case.get("idx_global", 0.0))
+    batch = msa.Batch(case["seq_lens"], case["block_table"], w.q_per_seq)
+    cfg = msa.default_config(w.topk)
+    iq = msa.Query(case["index_q"], w.q_dtype, case["index_q_scale"])
+    q = msa.Query(case["q"], w.q_dtype, case["q_scale"])
+    ws = torch.empty(msa.msa_workspace_size(cache, batch, cfg, w.num_q_heads), dtype=torch.uint8, device=dev)
+    msa.msa_workspace_init(ws)
+    rows = w.num_seqs * w.q_per_seq
+    topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((rows, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((rows, w.num_q_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, lse, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, flags = msa.msa_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {msa.msa_status_string(st)} flags {flags}")
+
+    # ---------------- timed region: K steps, L2 flushed before each, events around each step
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_step = sum(step_ms) / len(step_ms)
+
+    # dominant kernel (the indexer scan) timed alone on the same stream, same launch shape
+    pooled = torch.empty((rows, w.num_kv_heads, w.max_blocks), dtype=torch.float32, device=dev)
+    ievs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for _ in range(3):
+        msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws, stream)
+    for i in range(args.steps):
+        flush.zero_()
+        ievs[i][0].record(stream)
+        msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws, stream)
+        ievs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    idx_ms = sum(a.elapsed_time(b) for a, b in ievs) / args.steps
+
+    # ---------------- end to end through the public API with host buffers
+    h_iq = torch.empty_like(case["index_q"], device="cpu").pin_memory()
+    h_q = torch.empty_like(case["q"], device="cpu").pin_memory()
+    h_iq.copy_(case["index_q"].cpu())
+    h_q.copy_(case["q"].cpu())
+    h_lens = case["seq_lens"].cpu().pin_memory()
+    h_bt = case["block_table"].cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_topk = torch.empty(topk.shape, dtype=topk.dtype).pin_memory()
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_evs[i][0].record(stream)
+        case["index_q"].copy_(h_iq, non_blocking=True)
+        case["q"].copy_(h_q, non_blocking=True)
+        case["seq_lens"].copy_(h_lens, non_blocking=True)
+        case["block_table"].copy_(h_bt, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_topk.copy_(topk, non_blocking=True)
+        e2e_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_iq, h_q, h_lens, h_bt))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_topk))
+    st, flags = msa.msa_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {msa.msa_status_string(st)} flags {flags}")
+
+    # ---------------- byte model from this step's selection
+    sel = topk.cpu().numpy()
+    unions = []
+    for s in range(w.num_seqs):
+        per_g = []
+        for g in range(w.num_kv_heads):
+            blocks = set(int(b) for b in sel[s * w.q_per_seq:(s + 1) * w.q_per_seq, g].ravel() if b >= 0)
+            per_g.append(sorted(blocks))
+        unions.append(per_g)
+    idx_bytes, kv_bytes, actual_bytes = algorithmic_bytes(w, unions)
+    step_bytes = idx_bytes + kv_bytes
+    peak, peak_kind = load_peaks()
+
+    # max over ranks
+    vals = torch.tensor([ms_step, idx_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms_step, idx_ms, e2e_ms = (float(x) for x in vals.cpu())
+    queries = rows * world
+    qps = queries / (ms_step * 1e-3)
+    e2e_qps = queries / (e2e_ms * 1e-3)
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        h = ms.case_to_host(case) if args.workload != "fp8_long" else None
+        if h is not None:
+            nseq = 2
+            dt = cpu_oracle_sample(w, h, list(range(nseq)))
+            cpu_base = {"value": nseq * w.q_per_seq / dt, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                        "sample": f"first {nseq} of the {w.num_seqs} sequences, whole path in fp64 (numpy)"}
+        else:
+            ws1 = ms.make_workload(args.workload, seq_lens=(w.seq_lens[0],))
+            h1 = ms.case_to_host(ms.make_case(ws1, device="cpu"))
+            dt = cpu_oracle_sample(ws1, h1, [0])
+            cpu_base = {"value": 1 * ws1.q_per_seq / dt, "unit": "queries/s", "cores": 1, "kind": "oracle",
+                        "sample": "one 512K-token sequence regenerated on the host, whole path in fp64"}
+
+    if rank == 0:
+        idx_gbs = idx_bytes / (idx_ms * 1e-3) / 1e9
+        path_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 MMA, fp32 accumulate" if w.kv_dtype == "fp8" else w.kv_dtype,
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed (256 MB write) before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "path_hbm_gbs": path_gbs, "path_frac_of_peak": path_gbs / peak,
+            "bytes_per_step": {"algorithmic": step_bytes, "index": idx_bytes, "kv_selected": kv_bytes,
+                               "with_fp32_scales": actual_bytes},
+            "roofline": {"bound": "hbm", "kernel": "indexer (prep + score/pool launch)", "achieved": idx_gbs,
+                         "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                         "peak_kind": peak_kind},
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,451 @@
+// C ABI of libmsa (declared in include/msa.h): argument checks, workspace
+// carving, TMA descriptor encoding and the launch chains of each entry point.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+using namespace msa;
+
+namespace {
+
+// ---------------------------------------------------------------- device facts
+
+int sm_count() {
+  static int cache[64];
+  static bool init[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!init[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+    init[dev] = true;
+  }
+  return cache[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over rows of 128 elements (FP8: 128 B, BF16: 256 B); one box is
+// 128 rows x 128 bytes with the 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, long rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {bf16 ? 256ull : 128ull};
+  cuuint32_t box[2] = {bf16 ? 64u : 128u, 128u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fmt_of(msa_dtype_t d) {
+  switch (d) {
+    case MSA_DTYPE_BF16: return FMT_BF16;
+    case MSA_DTYPE_FP8_E4M3: return FMT_FP8;
+    case MSA_DTYPE_NVFP4: return FMT_NVFP4;
+    default: return -1;
+  }
+}
+
+int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+msa_status_t check_batch(const msa_batch_t* b) {
+  if (!b || !b->seq_lens || !b->block_table) return MSA_ERR_INVALID_ARGUMENT;
+  if (b->num_seqs < 1 || b->q_per_seq < 1 || b->max_blocks_per_seq < 1) return MSA_ERR_INVALID_ARGUMENT;
+  if ((long)b->max_blocks_per_seq * kBlock > (1l << 30)) return MSA_ERR_UNSUPPORTED;
+  if (b->q_per_seq > 32) return MSA_ERR_UNSUPPORTED;  // decode / verify path: up to 32 new tokens
+  return MSA_OK;
+}
+
+msa_status_t check_cfg(const msa_config_t* c) {
+  if (!c) return MSA_ERR_INVALID_ARGUMENT;
+  if (c->topk != 4 && c->topk != 8 && c->topk != 16 && c->topk != 32) return MSA_ERR_UNSUPPORTED;
+  if (c->init_blocks < 0 || c->local_blocks < 0 || c->init_blocks + c->local_blocks > c->topk - 1)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!(c->index_scale > 0.f) || !std::isfinite(c->index_scale)) return MSA_ERR_INVALID_ARGUMENT;
+  if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale)) return MSA_ERR_INVALID_ARGUMENT;
+  return MSA_OK;
+}
+
+msa_status_t check_cache(const msa_cache_t* c, bool need_index, bool need_kv) {
+  if (!c) return MSA_ERR_INVALID_ARGUMENT;
+  if (c->block_size != kBlock || c->head_dim != kDim || c->index_dim != kDim) return MSA_ERR_UNSUPPORTED;
+  if (c->num_kv_heads < 1 || c->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
+  if (c->num_blocks < 1 || (long)c->num_blocks * c->num_kv_heads * kBlock >= (1l << 31)) return MSA_ERR_UNSUPPORTED;
+  if (need_index) {
+    const int f = fmt_of(c->index_dtype);
+    if (f < 0) return MSA_ERR_UNSUPPORTED;
+    if (!c->idx || !aligned16(c->idx)) return MSA_ERR_INVALID_ARGUMENT;
+    if (f == FMT_FP8 && (!c->idx_scale || !aligned16(c->idx_scale))) return MSA_ERR_INVALID_ARGUMENT;
+    if (f == FMT_NVFP4 && (!c->idx_sf || !aligned16(c->idx_sf) || !(c->idx_global > 0.f))) return MSA_ERR_INVALID_ARGUMENT;
+  }
+  if (need_kv) {
+    const int f = fmt_of(c->kv_dtype);
+    if (f < 0) return MSA_ERR_UNSUPPORTED;
+    if (!c->k || !c->v || !aligned16(c->k) || !aligned16(c->v)) return MSA_ERR_INVALID_ARGUMENT;
+    if (f == FMT_FP8 && (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)))
+      return MSA_ERR_INVALID_ARGUMENT;
+    if (f == FMT_NVFP4 && (!c->k_sf || !c->v_sf || !aligned16(c->k_sf) || !aligned16(c->v_sf) ||
+                           !(c->k_global > 0.f) || !(c->v_global > 0.f)))
+      return MSA_ERR_INVALID_ARGUMENT;
+  }
+  return MSA_OK;
+}
+
+msa_status_t check_query(const msa_query_t* q) {
+  if (!q || !q->data || !aligned16(q->data)) return MSA_ERR_INVALID_ARGUMENT;
+  if (q->dtype != MSA_DTYPE_BF16 && q->dtype != MSA_DTYPE_FP8_E4M3) return MSA_ERR_UNSUPPORTED;
+  if (q->dtype == MSA_DTYPE_FP8_E4M3 && !(q->scale > 0.f && std::isfinite(q->scale))) return MSA_ERR_INVALID_ARGUMENT;
+  return MSA_OK;
+}
+
+// ---------------------------------------------------------------- workspace plan
+
+FragGeom geom_for(int key_fmt, bool q_fp8, int cols) {
+  FragGeom g;
+  g.cols = cols;
+  g.sp = (key_fmt == FMT_FP8 && !q_fp8) ? 2 : 1;
+  g.ks = (key_fmt == FMT_FP8) ? 4 : 8;
+  g.nt = next_pow2((cols + 7) / 8);
+  return g;
+}
+
+struct Plan {
+  FragGeom gi, ga;          // indexer / attend query geometry
+  int bps = 0, splits = 0, cap = 0, r = 0;
+  size_t off_status = 0, off_qfi = 0, off_cfi = 0, off_qfa = 0, off_cfa = 0, off_pooled = 0, off_uids = 0,
+         off_umask = 0, off_ucount = 0, off_po = 0, off_pml = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Plan for the given problem.  iq_fp8 / q_fp8: query dtypes (E4M3 or bf16).
+msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, int hq, bool iq_fp8,
+                       bool q_fp8, Plan& pl) {
+  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+  if (hq < G || hq % G != 0) return MSA_ERR_INVALID_ARGUMENT;
+  pl.r = hq / G;
+  const int fi = fmt_of(c->index_dtype), fa = fmt_of(c->kv_dtype);
+  pl.gi = geom_for(fi < 0 ? FMT_FP8 : fi, iq_fp8, Q * G);
+  pl.ga = geom_for(fa < 0 ? FMT_FP8 : fa, q_fp8, Q * pl.r);
+  if (pl.gi.nt > kMaxIndexerNT || pl.gi.nt * pl.gi.sp > 8) return MSA_ERR_UNSUPPORTED;
+  if (pl.ga.cols > kMaxAttendCols || pl.ga.nt * pl.ga.sp > 8) return MSA_ERR_UNSUPPORTED;
+  pl.bps = attend_max_stages(fa < 0 ? FMT_FP8 : fa);
+  pl.cap = Q * cfg->topk;
+  pl.splits = (pl.cap + pl.bps - 1) / pl.bps;
+  size_t o = 0;
+  pl.off_status = o; o = align256(o + 256);
+  pl.off_qfi = o; o = align256(o + (size_t)S * pl.gi.words_per_unit() * 4);
+  pl.off_cfi = o; o = align256(o + (size_t)S * pl.gi.nt * 8 * 4);
+  pl.off_qfa = o; o = align256(o + (size_t)S * G * pl.ga.words_per_unit() * 4);
+  pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
+  pl.off_pooled = o; o = align256(o + (size_t)S * Q * G * b->max_blocks_per_seq * 4);
+  pl.off_uids = o; o = align256(o + (size_t)S * G * pl.cap * 4);
+  pl.off_umask = o; o = align256(o + (size_t)S * G * pl.cap * 4);
+  pl.off_ucount = o; o = align256(o + (size_t)S * G * 4);
+  pl.off_po = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 128 * 4);
+  pl.off_pml = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 2 * 4);
+  pl.total = o;
+  return MSA_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+BatchDev batch_dev(const msa_batch_t* b) {
+  BatchDev d;
+  d.seq_lens = b->seq_lens;
+  d.block_table = b->block_table;
+  d.S = b->num_seqs;
+  d.Q = b->q_per_seq;
+  d.max_nb = b->max_blocks_per_seq;
+  return d;
+}
+
+msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+// ---------------------------------------------------------------- stages of the path
+
+msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* iq,
+                         const Plan& pl, void* ws, float* pooled, cudaStream_t st) {
+  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+  const int fi = fmt_of(c->index_dtype);
+  PrepParams pp;
+  pp.q = iq->data;
+  pp.q_is_fp8 = iq->dtype == MSA_DTYPE_FP8_E4M3;
+  pp.q_scale = pp.q_is_fp8 ? iq->scale : 1.f;
+  pp.col_const = cfg->index_scale * (fi == FMT_NVFP4 ? c->idx_global : 1.f);
+  pp.key_fmt = fi;
+  pp.geom = pl.gi;
+  pp.units = S;
+  pp.frag = at<uint32_t>(ws, pl.off_qfi);
+  pp.colf = at<float>(ws, pl.off_cfi);
+  cudaError_t e = launch_prep_rows(pp, Q * G, 1, 0, G, G, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  CUtensorMap tm;
+  const CUtensorMap* tmp = nullptr;
+  if (fi != FMT_NVFP4) {
+    if (!encode_rows(&tm, c->idx, (long)c->num_blocks * kBlock, fi == FMT_BF16)) return MSA_ERR_CUDA;
+    tmp = &tm;
+  }
+  IndexerParams ip;
+  ip.batch = batch_dev(b);
+  ip.G = G;
+  ip.num_blocks = c->num_blocks;
+  ip.idx = static_cast<const uint8_t*>(c->idx);
+  ip.idx_sf = static_cast<const uint8_t*>(c->idx_sf);
+  ip.idx_scale = c->idx_scale;
+  ip.qfrag = pp.frag;
+  ip.colf = pp.colf;
+  ip.geom = pl.gi;
+  ip.pooled = pooled;
+  ip.status = at<DeviceStatus>(ws, pl.off_status);
+  return cuda_status(launch_indexer(fi, tmp, ip, sm_count(), st, true));
+}
+
+msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, const float* pooled, int32_t* topk_idx,
+                      float* topk_score, void* ws, const Plan* pl, cudaStream_t st, bool pdl) {
+  TopkParams tp;
+  tp.batch = batch_dev(b);
+  tp.G = G;
+  tp.topk = cfg->topk;
+  tp.init_blocks = cfg->init_blocks;
+  tp.local_blocks = cfg->local_blocks;
+  tp.pooled = pooled;
+  tp.topk_idx = topk_idx;
+  tp.topk_score = topk_score;
+  tp.status = pl ? at<DeviceStatus>(ws, pl->off_status) : static_cast<DeviceStatus*>(ws);
+  return cuda_status(launch_topk(tp, st, pdl));
+}
+
+msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* q,
+                        int hq, const int32_t* topk_idx, void* out, float* lse, const Plan& pl, void* ws,
+                        cudaStream_t st, bool prep_done) {
+  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+  const int fa = fmt_of(c->kv_dtype);
+  DeviceStatus* status = at<DeviceStatus>(ws, pl.off_status);
+  if (!prep_done) {
+    PrepParams pp;
+    pp.q = q->data;
+    pp.q_is_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
+    pp.q_scale = pp.q_is_fp8 ? q->scale : 1.f;
+    pp.col_const = cfg->sm_scale * 1.4426950408889634f * (fa == FMT_NVFP4 ? c->k_global : 1.f);
+    pp.key_fmt = fa;
+    pp.geom = pl.ga;
+    pp.units = S * G;
+    pp.frag = at<uint32_t>(ws, pl.off_qfa);
+    pp.colf = at<float>(ws, pl.off_cfa);
+    if (launch_prep_rows(pp, Q * hq, G, pl.r, pl.r, hq, st) != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  UnionParams up;
+  up.batch = batch_dev(b);
+  up.G = G;
+  up.topk = cfg->topk;
+  up.topk_idx = topk_idx;
+  up.cap = pl.cap;
+  up.u_ids = at<int32_t>(ws, pl.off_uids);
+  up.u_mask = at<uint32_t>(ws, pl.off_umask);
+  up.u_count = at<int32_t>(ws, pl.off_ucount);
+  up.status = status;
+  if (launch_union(up, st, true) != cudaSuccess) return MSA_ERR_CUDA;
+
+  CUtensorMap tk, tv;
+  const CUtensorMap *tkp = nullptr, *tvp = nullptr;
+  if (fa != FMT_NVFP4) {
+    const long rows = (long)c->num_blocks * G * kBlock;
+    if (!encode_rows(&tk, c->k, rows, fa == FMT_BF16) || !encode_rows(&tv, c->v, rows, fa == FMT_BF16))
+      return MSA_ERR_CUDA;
+    tkp = &tk;
+    tvp = &tv;
+  }
+  AttendParams ap;
+  ap.batch = batch_dev(b);
+  ap.G = G;
+  ap.r = pl.r;
+  ap.num_blocks = c->num_blocks;
+  ap.k = static_cast<const uint8_t*>(c->k);
+  ap.v = static_cast<const uint8_t*>(c->v);
+  ap.k_sf = static_cast<const uint8_t*>(c->k_sf);
+  ap.v_sf = static_cast<const uint8_t*>(c->v_sf);
+  ap.k_scale = c->k_scale;
+  ap.v_scale = c->v_scale;
+  ap.v_global = c->v_global;
+  ap.qfrag = at<uint32_t>(ws, pl.off_qfa);
+  ap.colf = at<float>(ws, pl.off_cfa);
+  ap.geom = pl.ga;
+  ap.u_ids = up.u_ids;
+  ap.u_mask = up.u_mask;
+  ap.u_count = up.u_count;
+  ap.cap = pl.cap;
+  ap.bps = pl.bps;
+  ap.splits = pl.splits;
+  ap.part_o = at<float>(ws, pl.off_po);
+  ap.part_ml = at<float>(ws, pl.off_pml);
+  ap.status = status;
+  if (launch_attend(fa, tkp, tvp, ap, st, true) != cudaSuccess) return MSA_ERR_CUDA;
+
+  CombineParams cp;
+  cp.S = S;
+  cp.Q = Q;
+  cp.G = G;
+  cp.r = pl.r;
+  cp.splits = pl.splits;
+  cp.cols = pl.ga.cols;
+  cp.part_o = ap.part_o;
+  cp.part_ml = ap.part_ml;
+  cp.out = out;
+  cp.lse = lse;
+  return cuda_status(launch_combine(cp, st, true));
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARGUMENT: return "MSA_ERR_INVALID_ARGUMENT";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED";
+    case MSA_ERR_WORKSPACE_TOO_SMALL: return "MSA_ERR_WORKSPACE_TOO_SMALL";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA";
+    case MSA_ERR_DEVICE_FAULT: return "MSA_ERR_DEVICE_FAULT";
+    case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT";
+    default: return "MSA_ERR_UNKNOWN";
+  }
+}
+
+size_t msa_workspace_size(const msa_cache_t* cache, const msa_batch_t* batch, const msa_config_t* cfg,
+                          int32_t num_q_heads) {
+  if (check_batch(batch) != MSA_OK || check_cfg(cfg) != MSA_OK || check_cache(cache, false, false) != MSA_OK)
+    return 0;
+  // the largest plan over query dtypes (a bf16 query against FP8 keys needs two terms)
+  Plan pl;
+  if (make_plan(cache, batch, cfg, num_q_heads, false, false, pl) != MSA_OK) {
+    if (make_plan(cache, batch, cfg, num_q_heads, true, true, pl) != MSA_OK) return 0;
+  }
+  return pl.total;
+}
+
+msa_status_t msa_workspace_init(void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  if (!workspace || workspace_bytes < 256) return MSA_ERR_INVALID_ARGUMENT;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 256, (cudaStream_t)stream));
+}
+
+msa_status_t msa_indexer_score(const msa_cache_t* cache, const msa_batch_t* batch, const msa_config_t* cfg,
+                               const msa_query_t* index_q, float* pooled, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK || (s = check_cache(cache, true, false)) != MSA_OK ||
+      (s = check_query(index_q)) != MSA_OK)
+    return s;
+  if (!pooled || !workspace) return MSA_ERR_INVALID_ARGUMENT;
+  Plan pl;
+  if ((s = make_plan(cache, batch, cfg, cache->num_kv_heads, index_q->dtype == MSA_DTYPE_FP8_E4M3, false, pl)) != MSA_OK)
+    return s;
+  if (workspace_bytes < pl.off_pooled) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, (cudaStream_t)stream);
+}
+
+msa_status_t msa_topk_blocks(const msa_batch_t* batch, const msa_config_t* cfg, int32_t num_groups,
+                             const float* pooled, int32_t* topk_idx, float* topk_score, void* workspace,
+                             size_t workspace_bytes, msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK) return s;
+  if (num_groups < 1 || num_groups > 8 || !pooled || !topk_idx || !workspace) return MSA_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < 256) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_topk(batch, cfg, num_groups, pooled, topk_idx, topk_score, workspace, nullptr, (cudaStream_t)stream, false);
+}
+
+msa_status_t msa_sparse_attend(const msa_cache_t* cache, const msa_batch_t* batch, const msa_config_t* cfg,
+                               const msa_query_t* q, int32_t num_q_heads, const int32_t* topk_idx, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK || (s = check_cache(cache, false, true)) != MSA_OK ||
+      (s = check_query(q)) != MSA_OK)
+    return s;
+  if (!topk_idx || !out || !workspace || !aligned16(out)) return MSA_ERR_INVALID_ARGUMENT;
+  Plan pl;
+  if ((s = make_plan(cache, batch, cfg, num_q_heads, true, q->dtype == MSA_DTYPE_FP8_E4M3, pl)) != MSA_OK) return s;
+  if (workspace_bytes < pl.total) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, (cudaStream_t)stream, false);
+}
+
+msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, const msa_config_t* cfg,
+                        const msa_query_t* index_q, const msa_query_t* q, int32_t num_q_heads, int32_t* topk_idx,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK || (s = check_cache(cache, true, true)) != MSA_OK ||
+      (s = check_query(index_q)) != MSA_OK || (s = check_query(q)) != MSA_OK)
+    return s;
+  if (!topk_idx || !out || !workspace || !aligned16(out)) return MSA_ERR_INVALID_ARGUMENT;
+  Plan pl;
+  if ((s = make_plan(cache, batch, cfg, num_q_heads, index_q->dtype == MSA_DTYPE_FP8_E4M3,
+                     q->dtype == MSA_DTYPE_FP8_E4M3, pl)) != MSA_OK)
+    return s;
+  if (workspace_bytes < pl.total) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  float* pooled = at<float>(workspace, pl.off_pooled);
+  if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st)) != MSA_OK) return s;
+  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true)) != MSA_OK)
+    return s;
+  return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st, false);
+}
+
+msa_status_t msa_read_device_status(void* workspace, msa_stream_t stream, int32_t* detail) {
+  if (!workspace) return MSA_ERR_INVALID_ARGUMENT;
+  DeviceStatus h = {0, 0};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(h), st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (detail) *detail = (int32_t)h.flags;
+  if (h.flags & FLAG_TIMEOUT) return MSA_ERR_TIMEOUT;
+  if (h.flags) return MSA_ERR_DEVICE_FAULT;
+  return MSA_OK;
+}
+
+msa_status_t msa_dequant_debug(const msa_cache_t* cache, int32_t which, const int32_t* phys_blocks, int32_t n,
+                               float* out, msa_stream_t stream) {
+  if (which < 0 || which > 2 || n < 0 || (n > 0 && (!phys_blocks || !out))) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t s = check_cache(cache, which == 2, which != 2);
+  if (s != MSA_OK) return s;
+  const int f = fmt_of(which == 2 ? cache->index_dtype : cache->kv_dtype);
+  return cuda_status(launch_dequant(f, which, *cache, phys_blocks, n, out, (cudaStream_t)stream));
+}
+
+}  // extern "C"

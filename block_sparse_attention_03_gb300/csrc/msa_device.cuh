@@ -1,0 +1,229 @@
+// Device-side building blocks shared by the MSA kernels (sm_103a).
+//
+// - mbarrier + bulk / tensor (TMA) copies into shared memory, with every wait
+//   bounded: a wait that gives up sets MSA_FLAG_TIMEOUT in the status word and
+//   the caller skips the work instead of hanging;
+// - warp-level tensor-core MMA wrappers (mma.sync e4m3 k32 / bf16 k16 / f16 k16);
+// - small conversions (fp32 pairs -> packed e4m3 / bf16 / f16).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace msa {
+
+constexpr int kBlock = 128;  // tokens per paged block
+constexpr int kDim = 128;    // head_dim == index_dim
+
+// status word bits (sticky, first word of the workspace)
+constexpr uint32_t FLAG_BAD_BLOCK = 1u << 0;    // block-table entry outside the pool
+constexpr uint32_t FLAG_BAD_SEQLEN = 1u << 1;   // seq_len outside [q_per_seq, max_blocks*128]
+constexpr uint32_t FLAG_BAD_SELECT = 1u << 2;   // selected block the query cannot see
+constexpr uint32_t FLAG_TIMEOUT = 1u << 3;      // a bounded wait gave up
+
+struct DeviceStatus {
+  uint32_t flags;
+  int32_t detail;
+};
+
+__device__ __forceinline__ void raise_flag(DeviceStatus* st, uint32_t f, int32_t detail) {
+  if (st != nullptr) {
+    atomicOr(&st->flags, f);
+    atomicExch(&st->detail, detail);
+  }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Wait until the phase with the given parity completes.  Bounded: returns
+// false after ~max_tries polls (each poll may suspend up to ~20 us).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 200000) {
+  const uint32_t a = smem_u32(bar);
+  for (int i = 0; i < max_tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Warp-uniform wait: every lane polls, the warp agrees on the outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int max_tries = 200000) {
+  const uint32_t a = smem_u32(bar);
+  for (int i = 0; i < max_tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (__all_sync(0xffffffffu, done)) return true;
+  }
+  return false;
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (bulk / tensor copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared; both addresses 16-B aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tensor (TMA) copy global -> shared at element coordinates (x, y).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- PDL
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ---------------------------------------------------------------- MMA (warp-level)
+
+// D[16x8] += A[16x32] * B[32x8], e4m3 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_k32(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs.
+__device__ __forceinline__ void mma_bf16_k16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D[16x8] += A[16x16] * B[16x8], f16 inputs.
+__device__ __forceinline__ void mma_f16_k16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 b16 matrices from shared memory (row addresses from lanes 0-31).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// ---------------------------------------------------------------- conversions
+
+// Pack two floats into e4m3x2 (lo -> byte 0), round to nearest even, saturating.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; mov.b16 %0, t; }" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Decode two e4m3 bytes (byte 0 -> .x) to floats exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  uint32_t h;
+  asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(v));
+  __half2 hh = *reinterpret_cast<__half2*>(&h);
+  return __half22float2(hh);
+}
+
+// Decode one e4m3 byte exactly.
+__device__ __forceinline__ float e4m3_to_float(uint8_t v) { return e4m3x2_to_float2(v).x; }
+
+// Decode two e2m1 nibbles of one byte (low nibble -> .x) to f16x2 exactly.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h) : "r"(byte));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Split x (|x| <= 448) into e4m3 hi + lo with x ~= hi + lo to ~8 significant bits.
+__device__ __forceinline__ void split_e4m3(float x, float& hi, float& lo) {
+  uint16_t h = pack_e4m3x2(x, 0.f);
+  hi = e4m3x2_to_float2(h).x;
+  lo = x - hi;
+}
+
+// Largest e with amax * 2^e <= lim (amax > 0); 0 for amax == 0.
+__device__ __forceinline__ int pow2_fit(float amax, float lim) {
+  if (!(amax > 0.f)) return 0;
+  int e;
+  frexpf(lim / amax, &e);  // lim/amax = f * 2^e, f in [0.5, 1)
+  e -= 1;
+  while (ldexpf(amax, e) > lim) --e;
+  while (ldexpf(amax, e + 1) <= lim) ++e;
+  return e;
+}
+
+// Order-preserving map of a float to uint32 (NaN sorts as -inf - 1).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  if (f != f) return 0u;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float order_key_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+}  // namespace msa

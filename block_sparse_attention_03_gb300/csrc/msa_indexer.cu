@@ -1,0 +1,379 @@
+// Indexer score + block max-pool over the paged index-key cache (decode and
+// speculative verify: up to 64 (query x group) columns per sequence).
+//
+// Definition (vLLM Day-0 blog, section "MSA 入门"): every key t of the context
+// is scored against one index query per GQA group through the single shared
+// index-key head, s = scale * <index_q[g], key[t]>, and the scores are
+// max-pooled to one value per 128-token block; keys a query cannot see
+// (t > its position) do not take part.
+//
+// GB300 mapping.  The scan is HBM-bound (128 B/token for FP8 keys), but at
+// 4 groups x 128 dims it needs 4 MACs per byte, more than the FP32 pipe can
+// issue at HBM rate, so the dot products run on the tensor pipe:
+//   S^T[key][col] = Keys[128 x 128] * Q^T[128 x cols]   (mma.sync, keys = rows)
+// Each warp owns a private ring of NST shared-memory stages; lane 0 streams
+// whole 128-token blocks into it (TMA tensor copy with the 128-byte swizzle
+// for FP8/BF16, so ldmatrix reads are bank-conflict free; a 1-D bulk copy for
+// NVFP4, whose 64-byte rows are read conflict-free as they are).  Keys are fed
+// to the MMA without conversion (e4m3 / bf16) or dequantized exactly to f16 in
+// registers (NVFP4: e2m1 -> f16, times the e4m3 block scale, an exact product).
+// The per-token FP8 scale multiplies each row before the block max; the
+// column factor (query scale, power-of-two prescale, index scale, NVFP4
+// per-tensor scale: all positive) is applied after it.
+//
+// Work: unit = (sequence s, logical block b), b-major so that consecutive
+// units of a warp stay on one sequence when the warp count is a multiple of
+// the batch; units past a sequence's end write -inf.
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+
+namespace {
+
+template <int FMT>
+struct IdxTraits;
+
+template <>
+struct IdxTraits<FMT_FP8> {
+  static constexpr int KS = 4;               // k32 steps
+  static constexpr int TILE = 128 * 128;     // bytes of one block of keys
+  static constexpr int SCALES = 128 * 4;     // fp32 per-token scales
+  static constexpr int WARPS = 4, NST = 3;
+};
+template <>
+struct IdxTraits<FMT_BF16> {
+  static constexpr int KS = 8;
+  static constexpr int TILE = 128 * 256;     // two swizzled 128-byte halves
+  static constexpr int SCALES = 0;
+  static constexpr int WARPS = 2, NST = 2;
+};
+template <>
+struct IdxTraits<FMT_NVFP4> {
+  static constexpr int KS = 8;
+  static constexpr int TILE = 128 * 64;      // packed e2m1
+  static constexpr int SCALES = 128 * 8;     // e4m3 block scales
+  static constexpr int WARPS = 4, NST = 4;
+};
+
+// Shared-memory layout of one CTA: per warp NST tiles, NST scale buffers,
+// NST mbarriers and NST stage states; the tile region is 1024-byte aligned.
+template <int FMT>
+struct IdxLayout {
+  using T = IdxTraits<FMT>;
+  static constexpr int SC = T::SCALES > 16 ? T::SCALES : 16;
+  static constexpr size_t SCAL = (size_t)T::WARPS * T::NST * T::TILE;
+  static constexpr size_t BARS = SCAL + (size_t)T::WARPS * T::NST * SC;
+  static constexpr size_t STATE = BARS + (size_t)T::WARPS * T::NST * 8;
+  static constexpr size_t TOTAL = STATE + (size_t)T::WARPS * T::NST * 4;
+  static constexpr size_t SMEM = TOTAL + 1024;  // alignment slack
+};
+
+enum : int { ST_SKIP = 0, ST_LOADED = 1, ST_BAD = 2 };
+
+// Address of the 16-byte chunk `chunk` of row `row` in a 128-byte-row tile
+// written by TMA with the 128-byte swizzle (1024-byte aligned base).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int FMT, int NT, int SP>
+__device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* scales, const uint32_t (&bq)[SP][NT][IdxTraits<FMT>::KS][2],
+                                            int lane, int key0, const int lim_col[NT][2], float (&cmax)[NT][2]) {
+  constexpr int KS = IdxTraits<FMT>::KS;
+  const int g = lane >> 2, j = lane & 3;
+  const uint32_t tb = smem_u32(tile);
+#pragma unroll 1
+  for (int m = 0; m < 8; ++m) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
+      const int row = 16 * m + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        if constexpr (FMT == FMT_FP8) {
+          ldmatrix_x4(a, swz(tb, row, 2 * ks + (lane >> 4)));
+#pragma unroll
+          for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_e4m3_k32(acc[nt], a, bq[sp][nt][ks][0], bq[sp][nt][ks][1]);
+        } else {
+          const uint32_t half = tb + (ks >> 2) * (128 * 128);
+          ldmatrix_x4(a, swz(half, row, 2 * (ks & 3) + (lane >> 4)));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_k16(acc[nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+        }
+      }
+    } else {  // NVFP4: dequantize rows g and g+8 of this m-tile to f16 in registers
+      const int r0 = 16 * m + g, r1 = r0 + 8;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r0 * 64 + 16 * j);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r1 * 64 + 16 * j);
+      const uint16_t sc0 = *reinterpret_cast<const uint16_t*>(scales + r0 * 8 + 2 * j);
+      const uint16_t sc1 = *reinterpret_cast<const uint16_t*>(scales + r1 * 8 + 2 * j);
+      uint32_t s0[2], s1[2];
+      {
+        uint32_t h;
+        asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc0));
+        s0[0] = (h & 0xffffu) | (h << 16);
+        s0[1] = (h >> 16) | (h & 0xffff0000u);
+        asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc1));
+        s1[0] = (h & 0xffffu) | (h << 16);
+        s1[1] = (h >> 16) | (h & 0xffff0000u);
+      }
+      const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+      const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        // byte 2ks and 2ks+1 of the lane's 16 bytes hold dims 32j+4ks .. +3
+        const int bi = 2 * ks;
+        const uint32_t grp = bi >> 3;  // 0: dims 32j..+15, 1: 32j+16..+31
+        uint32_t a[4];
+        uint32_t x0 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+        uint32_t x2 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+        uint32_t x1 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+        uint32_t x3 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+        __half2 t;
+        t = __hmul2(*reinterpret_cast<__half2*>(&x0), *reinterpret_cast<const __half2*>(&s0[grp]));
+        a[0] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x1), *reinterpret_cast<const __half2*>(&s1[grp]));
+        a[1] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x2), *reinterpret_cast<const __half2*>(&s0[grp]));
+        a[2] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[grp]));
+        a[3] = *reinterpret_cast<uint32_t*>(&t);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_k16(acc[nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+      }
+    }
+    // epilogue: rows r0 = 16m + g, r1 = r0 + 8 of this block
+    const int r0 = 16 * m + g, r1 = r0 + 8;
+    float s0 = 1.f, s1 = 1.f;
+    if constexpr (FMT == FMT_FP8) {
+      s0 = reinterpret_cast<const float*>(scales)[r0];
+      s1 = reinterpret_cast<const float*>(scales)[r1];
+    }
+    const int t0 = key0 + r0, t1 = key0 + r1;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float v0 = (t0 <= lim_col[nt][c]) ? acc[nt][c] * s0 : -INFINITY;
+        const float v1 = (t1 <= lim_col[nt][c]) ? acc[nt][2 + c] * s1 : -INFINITY;
+        cmax[nt][c] = fmaxf(cmax[nt][c], fmaxf(v0, v1));
+      }
+  }
+}
+
+template <int FMT, int NT, int SP>
+__global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap, const IndexerParams p) {
+  using TR = IdxTraits<FMT>;
+  constexpr int KS = TR::KS, NST = TR::NST, WARPS = TR::WARPS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  using LY = IdxLayout<FMT>;
+  uint8_t* tiles = base + (size_t)warp * NST * TR::TILE;
+  uint8_t* scal = base + LY::SCAL + (size_t)warp * NST * LY::SC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + LY::BARS) + warp * NST;
+  int* state = reinterpret_cast<int*>(base + LY::STATE) + warp * NST;
+
+  const BatchDev bt = p.batch;
+  const int S = bt.S, Q = bt.Q, G = p.G;
+  const long total = (long)S * bt.max_nb;
+  const long gw = (long)blockIdx.x * WARPS + warp;
+  const long tw = (long)gridDim.x * WARPS;
+
+  if (lane == 0) {
+    for (int st = 0; st < NST; ++st) mbar_init(&bars[st], 1);
+    fence_mbar_init();
+    if constexpr (FMT != FMT_NVFP4) prefetch_tmap(&tmap);
+  }
+  __syncwarp();
+
+  // lane 0: decide and issue the copy of unit u into stage st
+  auto issue = [&](long u, int st) {
+    const int s = (int)(u % S), b = (int)(u / S);
+    const int T = __ldg(bt.seq_lens + s);
+    int stt = ST_SKIP;
+    if (T < Q || T > bt.max_nb * kBlock) {
+      if (b == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
+      stt = ST_BAD;
+    } else if (b < (T + kBlock - 1) / kBlock) {
+      const int phys = __ldg(bt.block_table + (size_t)s * bt.max_nb + b);
+      if (phys < 0 || phys >= p.num_blocks) {
+        raise_flag(p.status, FLAG_BAD_BLOCK, phys);
+        stt = ST_BAD;
+      } else {
+        stt = ST_LOADED;
+        uint8_t* dst = tiles + (size_t)st * TR::TILE;
+        fence_proxy_async();
+        if constexpr (FMT == FMT_FP8) {
+          mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
+          tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
+          bulk_g2s(scal + (size_t)st * LY::SC, p.idx_scale + (size_t)phys * kBlock, TR::SCALES, &bars[st]);
+        } else if constexpr (FMT == FMT_BF16) {
+          mbar_expect_tx(&bars[st], TR::TILE);
+          tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
+          tma_load_2d(dst + 128 * 128, &tmap, 64, phys * kBlock, &bars[st]);
+        } else {
+          mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
+          bulk_g2s(dst, p.idx + (size_t)phys * TR::TILE, TR::TILE, &bars[st]);
+          bulk_g2s(scal + (size_t)st * LY::SC, p.idx_sf + (size_t)phys * TR::SCALES, TR::SCALES, &bars[st]);
+        }
+      }
+    }
+    state[st] = stt;
+  };
+
+  if (lane == 0)
+    for (int st = 0; st < NST; ++st)
+      if (gw + (long)st * tw < total) issue(gw + (long)st * tw, st);
+  __syncwarp();
+  // the query fragments come from the preceding kernel (programmatic launch)
+  pdl_wait();
+
+  uint32_t phase_bits = 0;
+  int cur_s = -1;
+  uint32_t bq[SP][NT][KS][2];
+  float colf[NT][2];
+  bool dead = false;
+
+  int it = 0;
+  for (long u = gw; u < total; u += tw, ++it) {
+    const int st = it % NST;
+    const int s = (int)(u % S), b = (int)(u / S);
+    const int stt = state[st];
+    float* prow = p.pooled + (size_t)s * Q * G * bt.max_nb + b;
+    if (stt == ST_LOADED && !dead) {
+      if (s != cur_s) {
+        cur_s = s;
+        const uint32_t* fr = p.qfrag + (size_t)s * p.geom.words_per_unit();
+#pragma unroll
+        for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+              for (int rg = 0; rg < 2; ++rg)
+                bq[sp][nt][ks][rg] = __ldg(fr + ((((sp * NT + nt) * KS + ks) * 2 + rg) * 32) + lane);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) colf[nt][c] = __ldg(p.colf + (size_t)s * NT * 8 + nt * 8 + 2 * (lane & 3) + c);
+      }
+      const int T = __ldg(bt.seq_lens + s);
+      int lim[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = nt * 8 + 2 * (lane & 3) + c;
+          lim[nt][c] = (col < Q * G) ? (T - Q + col / G) : -1;
+        }
+      const bool ok = mbar_wait_warp(&bars[st], (phase_bits >> st) & 1u);
+      phase_bits ^= 1u << st;
+      if (!ok) {
+        if (lane == 0) raise_flag(p.status, FLAG_TIMEOUT, (int)u);
+        dead = true;
+      } else {
+        float cmax[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) cmax[nt][0] = cmax[nt][1] = -INFINITY;
+        score_block<FMT, NT, SP>(tiles + (size_t)st * TR::TILE, scal + (size_t)st * LY::SC, bq,
+                                 lane, b * kBlock, lim, cmax);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float v = cmax[nt][c];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            const int col = nt * 8 + 2 * (lane & 3) + c;
+            if (lane < 4 && col < Q * G) prow[(size_t)col * bt.max_nb] = v * colf[nt][c];
+          }
+      }
+    } else if (stt != ST_LOADED || dead) {
+      for (int col = lane; col < Q * G; col += 32) prow[(size_t)col * bt.max_nb] = -INFINITY;
+    }
+    __syncwarp();
+    if (!dead && lane == 0 && u + (long)NST * tw < total) issue(u + (long)NST * tw, st);
+    __syncwarp();
+  }
+  pdl_launch_dependents();
+  // a warp that gave up waits (bounded) for copies still in flight before exiting
+  if (dead) {
+    for (int st = 0; st < NST; ++st) mbar_wait(&bars[st], (phase_bits >> st) & 1u, 2000);
+  }
+}
+
+template <int FMT, int NT, int SP>
+cudaError_t launch_one(const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st, bool pdl) {
+  using TR = IdxTraits<FMT>;
+  const size_t smem = IdxLayout<FMT>::SMEM;
+  auto kern = indexer_kernel<FMT, NT, SP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, TR::WARPS * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const long units = (long)p.batch.S * p.batch.max_nb;
+  long grid = (long)num_sms * per_sm;
+  const long need = (units + TR::WARPS - 1) / TR::WARPS;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(TR::WARPS * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  CUtensorMap dummy = {};
+  return cudaLaunchKernelEx(&cfg, kern, tmap ? *tmap : dummy, p);
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st, bool pdl) {
+  const int nt = p.geom.nt, sp = p.geom.sp;
+  if (sp == 2) {
+    if constexpr (FMT == FMT_FP8) {
+      switch (nt) {
+        case 1: return launch_one<FMT, 1, 2>(tmap, p, num_sms, st, pdl);
+        case 2: return launch_one<FMT, 2, 2>(tmap, p, num_sms, st, pdl);
+        case 4: return launch_one<FMT, 4, 2>(tmap, p, num_sms, st, pdl);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    return cudaErrorInvalidValue;
+  }
+  switch (nt) {
+    case 1: return launch_one<FMT, 1, 1>(tmap, p, num_sms, st, pdl);
+    case 2: return launch_one<FMT, 2, 1>(tmap, p, num_sms, st, pdl);
+    case 4: return launch_one<FMT, 4, 1>(tmap, p, num_sms, st, pdl);
+    case 8: return launch_one<FMT, 8, 1>(tmap, p, num_sms, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
+                           bool pdl) {
+  switch (fmt) {
+    case FMT_FP8: return launch_fmt<FMT_FP8>(tmap, p, num_sms, st, pdl);
+    case FMT_BF16: return launch_fmt<FMT_BF16>(tmap, p, num_sms, st, pdl);
+    case FMT_NVFP4: return launch_fmt<FMT_NVFP4>(tmap, p, num_sms, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace msa

@@ -1,0 +1,271 @@
+// Top-k block selection and the per-(sequence, group) union of selections.
+//
+// Selection (vLLM Day-0 blog, section "MSA 入门"): per (query, group) keep
+// the top-k blocks by pooled indexer score, the most recent block always
+// kept.  Readings the pages leave open: the query's own block counts as one of
+// the k; the indexer constructor's init_blocks / local_blocks (model page,
+// MiniMaxM3SparseAttention.__init__) force the first blocks and the blocks
+// just before the query's block; equal scores keep the smaller block id; the
+// output is ascending and padded with -1.
+//
+// Kernel: one CTA per (query row, group).  The free candidates form one
+// contiguous id range [lo, hi) (everything between the forced init and local
+// blocks), so a radix select over order-preserving 32-bit keys (4 passes of
+// 8 bits, shared-memory histograms) finds the k'-th largest score; ties at the
+// threshold are resolved by id through a block-wide prefix count, and the
+// final ids come out ascending without a sort because each thread owns a
+// contiguous id range.
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kTopkThreads = 256;
+
+// block-wide exclusive scan of one int per thread; returns the total
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& excl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kTopkThreads / 32; ++w) {
+    const int t = warp_tot[w];
+    if (w < warp) wbase += t;
+    total += t;
+  }
+  excl = wbase + x - v;
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
+  __shared__ int hist[256];
+  __shared__ int warp_tot[kTopkThreads / 32];
+  __shared__ uint32_t sh_prefix, sh_need;
+
+  pdl_wait();
+  const BatchDev bt = p.batch;
+  const int row = blockIdx.x;  // (s*Q + i) * G + g
+  const int sq = row / p.G;
+  const int s = sq / bt.Q, i = sq % bt.Q;
+  const int T = bt.seq_lens[s];
+  const int K = p.topk;
+  int32_t* out = p.topk_idx + (size_t)row * K;
+  float* out_sc = p.topk_score ? p.topk_score + (size_t)row * K : nullptr;
+  const float* pr = p.pooled + (size_t)row * bt.max_nb;
+
+  if (T < bt.Q || T > bt.max_nb * kBlock) {
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      out[k] = -1;
+      if (out_sc) out_sc[k] = -INFINITY;
+    }
+    if (threadIdx.x == 0 && i == 0 && row % p.G == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
+    pdl_launch_dependents();
+    return;
+  }
+  const int pos = T - bt.Q + i;
+  const int recent = pos / kBlock;
+  const int n_init = min(p.init_blocks, recent);           // forced [0, n_init)
+  const int n_local = min(p.local_blocks, recent - n_init); // forced [recent - n_local, recent)
+  const int lo = n_init, hi = recent - n_local;            // free candidates [lo, hi)
+  const int ncand = hi - lo;
+  const int kfree = K - n_init - n_local - 1;
+
+  // thread-owned contiguous candidate range
+  const int per = (ncand + kTopkThreads - 1) / kTopkThreads;
+  const int b0 = lo + threadIdx.x * per;
+  const int b1 = min(hi, b0 + per);
+
+  uint32_t thr = 0;     // keys > thr are taken; keys == thr: the first `need_eq` by id
+  int need_eq = 0;
+  const bool take_all = ncand <= kfree;
+  const bool take_none = !take_all && kfree <= 0;
+  if (!take_all && !take_none) {
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = kfree;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int k = threadIdx.x; k < 256; k += blockDim.x) hist[k] = 0;
+      __syncthreads();
+      for (int b = b0; b < b1; ++b) {
+        const uint32_t key = float_order_key(pr[b]);
+        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        // lane l owns digits [8l, 8l+8); suffix sums from the top digit down
+        const int lane = threadIdx.x;
+        int own = 0;
+        for (int k = 0; k < 8; ++k) own += hist[8 * lane + k];
+        int suf = own;  // inclusive suffix over lanes >= lane
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, suf, o);
+          if (lane + o < 32) suf += y;
+        }
+        const int above = suf - own;  // count in lanes > lane
+        if (above < remaining && suf >= remaining) {
+          int acc = above;
+          for (int k = 7; k >= 0; --k) {
+            const int h = hist[8 * lane + k];
+            if (acc + h >= remaining) {
+              sh_prefix = prefix | ((uint32_t)(8 * lane + k) << shift);
+              sh_need = (uint32_t)(remaining - acc);
+              break;
+            }
+            acc += h;
+          }
+        }
+      }
+      __syncthreads();
+      prefix = sh_prefix;
+      remaining = (int)sh_need;
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;
+    need_eq = remaining;
+  }
+
+  // count this thread's takes, in id order
+  int n_gt = 0, n_eq = 0;
+  if (!take_all && !take_none) {
+    for (int b = b0; b < b1; ++b) {
+      const uint32_t key = float_order_key(pr[b]);
+      n_gt += key > thr;
+      n_eq += key == thr;
+    }
+  }
+  int eq_before = 0;
+  block_exclusive_scan(n_eq, warp_tot, eq_before);
+  const int eq_take = (take_all || take_none) ? 0 : max(0, min(n_eq, need_eq - eq_before));
+  const int my_take = take_all ? (b1 > b0 ? b1 - b0 : 0) : (take_none ? 0 : n_gt + eq_take);
+  int base = 0;
+  const int n_sel = block_exclusive_scan(my_take, warp_tot, base);
+
+  // ascending output: [0, n_init) ++ selected ++ [hi, recent]
+  int o = n_init + base;
+  int eq_seen = 0;
+  for (int b = b0; b < b1 && !take_none; ++b) {
+    const float v = pr[b];
+    bool take = take_all;
+    if (!take_all) {
+      const uint32_t key = float_order_key(v);
+      if (key > thr) take = true;
+      else if (key == thr) take = (eq_seen++ < eq_take);
+    }
+    if (take) {
+      out[o] = b;
+      if (out_sc) out_sc[o] = v;
+      ++o;
+    }
+  }
+  const int tail0 = n_init + n_sel;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    if (k < n_init) {
+      out[k] = k;
+      if (out_sc) out_sc[k] = pr[k];
+    } else if (k >= tail0) {
+      const int b = hi + (k - tail0);
+      const bool real = b <= recent;
+      out[k] = real ? b : -1;
+      if (out_sc) out_sc[k] = real ? pr[b] : -INFINITY;
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// Union of the Q queries' selections of one (sequence, group), ascending, with
+// a bit mask of the queries that chose each block.
+__global__ void __launch_bounds__(256) union_kernel(const UnionParams p) {
+  extern __shared__ int sh[];
+  int* ids = sh;                                      // [cap]
+  int* first = sh + p.cap;                            // [cap] 1 if first occurrence
+  uint32_t* masks = reinterpret_cast<uint32_t*>(sh + 2 * p.cap);  // [cap]
+  pdl_wait();
+  const BatchDev bt = p.batch;
+  const int unit = blockIdx.x;  // s * G + g
+  const int s = unit / p.G, g = unit % p.G;
+  const int T = bt.seq_lens[s];
+  const int n = bt.Q * p.topk;
+  const bool seq_ok = !(T < bt.Q || T > bt.max_nb * kBlock);
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int i = e / p.topk, k = e % p.topk;
+    int b = p.topk_idx[((size_t)(s * bt.Q + i) * p.G + g) * p.topk + k];
+    if (b >= 0) {
+      const int pos = T - bt.Q + i;
+      if (!seq_ok || b > pos / kBlock) {
+        if (seq_ok) raise_flag(p.status, FLAG_BAD_SELECT, b);
+        b = -1;
+      }
+    }
+    ids[e] = b;
+    masks[e] = 0;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int b = ids[e];
+    int f = b >= 0;
+    for (int e2 = 0; e2 < e && f; ++e2) f = ids[e2] != b;
+    first[e] = f;
+  }
+  __syncthreads();
+  // position of each unique block = number of unique blocks with a smaller id
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int b = ids[e];
+    if (b < 0) continue;
+    int rank = 0;
+    for (int e2 = 0; e2 < n; ++e2) rank += first[e2] && ids[e2] >= 0 && ids[e2] < b;
+    atomicOr(&masks[rank], 1u << (e / p.topk));
+    if (first[e]) p.u_ids[(size_t)unit * p.cap + rank] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int cnt = 0;
+    for (int e = 0; e < n; ++e) cnt += first[e];
+    p.u_count[unit] = cnt;
+  }
+  for (int e = threadIdx.x; e < n; e += blockDim.x) p.u_mask[(size_t)unit * p.cap + e] = masks[e];
+  pdl_launch_dependents();
+}
+
+cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const unsigned rows = (unsigned)(p.batch.S * p.batch.Q * p.G);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(kTopkThreads), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+}
+
+cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const size_t smem = (size_t)p.cap * 12;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)(p.batch.S * p.G)), dim3(256), smem, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, union_kernel, p);
+}
+
+}  // namespace msa

@@ -1,0 +1,221 @@
+/*
+ * msa.h -- C ABI of libmsa: the MiniMax Sparse Attention (MSA) decode hot path
+ * on one GB300 (sm_103a).
+ *
+ * What the path computes (vLLM blog "vLLM 实现 MiniMax-M3.1-Flash 的 Day-0 支持",
+ * section "MSA 入门" and its Figure 1):
+ *   1. a lightweight indexer scores every key of the paged context with one
+ *      index query per GQA group against one shared 128-dim index-key head;
+ *   2. the per-key scores are max-pooled to one score per 128-token block;
+ *   3. per group the top-k blocks (k = 16 in the model) are kept, the most
+ *      recent block always among them;
+ *   4. exact softmax attention runs for every query head of the group over
+ *      only the selected blocks (at most k x 128 keys).
+ * The index scale and the softmax scale are both head_dim ** -0.5 in the model
+ * (API page "vllm.models.minimax_m3.nvidia.model", MiniMaxM3SparseAttention:
+ * the indexer is built with scale=self.scaling).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer inside the structs and every tensor argument is DEVICE
+ *   memory of the current CUDA device unless stated otherwise.  The caller
+ *   owns every buffer, the workspace included; the library allocates nothing
+ *   and keeps no state beyond cached device attributes.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and never synchronise the host, except msa_read_device_status.
+ * - Host-checkable problems (null pointers, unsupported sizes or dtypes, a
+ *   workspace that is too small) return an error before any launch.
+ *   Launch failures return MSA_ERR_CUDA.  Data-dependent faults found on the
+ *   device (a block-table entry outside [0, num_blocks), a sequence length
+ *   outside [q_per_seq, max_blocks_per_seq * 128], a selected block id the
+ *   query cannot see) set a sticky status word in the workspace; the kernels
+ *   skip the offending work (outputs for it are left as documented below)
+ *   and never trap.  msa_read_device_status reports and clears that word.
+ * - Query token i (0-based) of the q_per_seq new tokens of sequence s sits at
+ *   position seq_lens[s] - q_per_seq + i; its keys are already in the cache.
+ *   Key t is visible to it iff t <= that position.
+ * - Rows of per-query tensors are token-major: row = s * q_per_seq + i.
+ *
+ * Paged-cache layout (one physical block = 128 tokens; all dims = 128):
+ *   K, V        BF16 / FP8: [num_blocks][num_kv_heads][128][head_dim] elements
+ *               NVFP4: [num_blocks][num_kv_heads][128][head_dim/2] bytes, element
+ *               2j in the low nibble of byte j; e4m3 scales k_sf / v_sf
+ *               [num_blocks][num_kv_heads][128][head_dim/16] (one per 16
+ *               consecutive elements), fp32 per-tensor k_global / v_global.
+ *   FP8 scales  k_scale, v_scale: fp32 [num_blocks][num_kv_heads][128]
+ *               (value = e4m3 * scale of its token and head).
+ *   index keys  one shared head: [num_blocks][128][index_dim] (BF16 / FP8) or
+ *               [num_blocks][128][index_dim/2] bytes + idx_sf
+ *               [num_blocks][128][index_dim/16] (NVFP4); FP8 per-token fp32
+ *               idx_scale [num_blocks][128]; NVFP4 per-tensor idx_global.
+ *   The index cache is addressed with the same block table as K/V.
+ *   Every base pointer must be 16-byte aligned.
+ * Formats: FP8 = OCP E4M3 ("FN": bias 7, no inf); NVFP4 = e2m1 values, one
+ * e4m3 scale per 16 elements, one fp32 per-tensor scale (Day-0 blog, section
+ * "MiniMax-M3.1 架构中的新特性").  The fp32 value of an NVFP4 element is
+ * fp32(e2m1 * e4m3_scale) * global (the inner product is exact in fp32).
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_BLOCK_SIZE 128
+#define MSA_HEAD_DIM 128
+
+typedef struct CUstream_st* msa_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, misaligned base */
+  MSA_ERR_UNSUPPORTED = 2,        /* valid but not implemented (dtype, topk, dims) */
+  MSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MSA_ERR_CUDA = 4,               /* a CUDA launch or copy failed */
+  MSA_ERR_DEVICE_FAULT = 5,       /* a kernel found bad data (see status word) */
+  MSA_ERR_TIMEOUT = 6             /* a bounded on-device wait gave up */
+} msa_status_t;
+
+typedef enum {
+  MSA_DTYPE_BF16 = 0,
+  MSA_DTYPE_FP8_E4M3 = 1,
+  MSA_DTYPE_NVFP4 = 2
+} msa_dtype_t;
+
+/* The paged K/V cache and the index-key side cache of one attention layer.
+ * K/V dtype and index dtype are independent (the model's
+ * --kv-cache-dtype and indexer_kv_dtype settings).  Unused pointers (scales of
+ * another format) may be NULL. */
+typedef struct {
+  msa_dtype_t kv_dtype;
+  msa_dtype_t index_dtype;
+  int32_t num_blocks;   /* physical blocks in the pool */
+  int32_t block_size;   /* must be 128 */
+  int32_t num_kv_heads; /* = number of GQA groups = number of index queries per token */
+  int32_t head_dim;     /* must be 128 */
+  int32_t index_dim;    /* must be 128 */
+  const void* k;
+  const void* v;
+  const void* k_sf;     /* NVFP4 only */
+  const void* v_sf;     /* NVFP4 only */
+  const float* k_scale; /* FP8 only */
+  const float* v_scale; /* FP8 only */
+  const void* idx;
+  const void* idx_sf;     /* NVFP4 only */
+  const float* idx_scale; /* FP8 only */
+  float k_global;       /* NVFP4 only */
+  float v_global;
+  float idx_global;
+} msa_cache_t;
+
+/* The batch: num_seqs sequences with q_per_seq new query tokens each.
+ * seq_lens[s] counts every token of sequence s, the new ones included.
+ * block_table[s][b] is the physical block holding logical block b of s. */
+typedef struct {
+  int32_t num_seqs;
+  int32_t q_per_seq;
+  int32_t max_blocks_per_seq;   /* row stride of block_table */
+  const int32_t* seq_lens;      /* device int32 [num_seqs] */
+  const int32_t* block_table;   /* device int32 [num_seqs][max_blocks_per_seq] */
+} msa_batch_t;
+
+/* Method settings (the indexer's constructor arguments in the model). */
+typedef struct {
+  int32_t topk;         /* blocks kept per (query, group): 4, 8, 16 or 32 */
+  int32_t init_blocks;  /* leading blocks always kept (model default 0) */
+  int32_t local_blocks; /* blocks just before the query's own block always kept (default 0) */
+  float index_scale;    /* multiplies the index scores; model: index_dim ** -0.5 */
+  float sm_scale;       /* softmax scale; model: head_dim ** -0.5 */
+} msa_config_t;
+
+/* A query tensor: BF16, or FP8 E4M3 codes times one fp32 per-tensor scale. */
+typedef struct {
+  const void* data;
+  msa_dtype_t dtype; /* MSA_DTYPE_BF16 or MSA_DTYPE_FP8_E4M3 */
+  float scale;       /* FP8 only */
+} msa_query_t;
+
+/* Bytes of workspace msa_decode (and each of the other entry points) needs
+ * for this problem.  Host-only; returns 0 for an invalid description. */
+size_t msa_workspace_size(const msa_cache_t* cache, const msa_batch_t* batch,
+                          const msa_config_t* cfg, int32_t num_q_heads);
+
+/* Clear the device status word at the start of a (fresh) workspace.  Call once
+ * after allocating a workspace; the word is sticky across calls until read. */
+msa_status_t msa_workspace_init(void* workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* Indexer score + block max-pool (steps 1-2 above).
+ * index_q: [num_seqs * q_per_seq][num_kv_heads][index_dim].
+ * pooled:  fp32 [num_seqs * q_per_seq][num_kv_heads][max_blocks_per_seq];
+ *          pooled[row][g][b] = index_scale * max over the keys t of block b
+ *          visible to that query of <index_q[row][g], index_key[t]>, and -inf
+ *          for a block with no visible key (and for b >= the sequence's block
+ *          count).  Rows of a sequence with a device fault are left -inf. */
+msa_status_t msa_indexer_score(const msa_cache_t* cache, const msa_batch_t* batch,
+                               const msa_config_t* cfg, const msa_query_t* index_q,
+                               float* pooled, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream);
+
+/* Top-k block selection (step 3) from pooled scores laid out as above.
+ * topk_idx:   int32 [num_seqs * q_per_seq][num_groups][topk], the query's own
+ *             block ⌊pos/128⌋ always included (forced, together with the
+ *             init/local blocks), the remaining slots filled with the highest
+ *             pooled scores of the earlier blocks (equal scores: smaller block
+ *             id first), ascending, padded with -1 when fewer blocks exist.
+ * topk_score: optional fp32 [same shape], the pooled score of each entry
+ *             (-inf for padding); may be NULL. */
+msa_status_t msa_topk_blocks(const msa_batch_t* batch, const msa_config_t* cfg,
+                             int32_t num_groups, const float* pooled, int32_t* topk_idx,
+                             float* topk_score, void* workspace, size_t workspace_bytes,
+                             msa_stream_t stream);
+
+/* Sparse attend (step 4): for query head h of group g = h / (num_q_heads /
+ * num_kv_heads), exact softmax attention over the visible keys of the blocks
+ * topk_idx[row][g][*] (entries < 0 are skipped), logits scaled by sm_scale.
+ * q:   [num_seqs * q_per_seq][num_q_heads][head_dim].
+ * out: bf16 [num_seqs * q_per_seq][num_q_heads][head_dim] (caller-allocated).
+ * lse: optional fp32 [num_seqs * q_per_seq][num_q_heads], natural-log
+ *      log-sum-exp of the scaled logits; may be NULL.
+ * A row whose selection holds no visible key gets out = 0, lse = -inf. */
+msa_status_t msa_sparse_attend(const msa_cache_t* cache, const msa_batch_t* batch,
+                               const msa_config_t* cfg, const msa_query_t* q,
+                               int32_t num_q_heads, const int32_t* topk_idx, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream);
+
+/* The whole path in one call on one stream (score -> pool -> top-k -> attend),
+ * no host synchronisation.  topk_idx (output, layout as in msa_topk_blocks)
+ * receives the selection; out / lse as in msa_sparse_attend. */
+msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch,
+                        const msa_config_t* cfg, const msa_query_t* index_q,
+                        const msa_query_t* q, int32_t num_q_heads, int32_t* topk_idx,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        msa_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace's status word.
+ * Returns MSA_OK, MSA_ERR_DEVICE_FAULT or MSA_ERR_TIMEOUT; *detail (optional,
+ * host pointer) receives the raw flag bits. */
+msa_status_t msa_read_device_status(void* workspace, msa_stream_t stream, int32_t* detail);
+
+/* Static, human-readable name of a status code. */
+const char* msa_status_string(msa_status_t status);
+
+/* Test hook: the fp32 value of every element of the given physical blocks.
+ * which: 0 = K, 1 = V (out fp32 [n][num_kv_heads][128][head_dim]),
+ *        2 = index keys (out fp32 [n][128][index_dim]).
+ * phys_blocks: device int32 [n].  Entries outside [0, num_blocks) produce NaN
+ * rows.  The values are bit-identical to the definition in the format notes
+ * above (one fp32 rounding for FP8 and NVFP4). */
+msa_status_t msa_dequant_debug(const msa_cache_t* cache, int32_t which,
+                               const int32_t* phys_blocks, int32_t n, float* out,
+                               msa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

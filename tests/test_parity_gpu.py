@@ -1,0 +1,188 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Every case generates its inputs once on the GPU (seeded), runs the library,
+copies the inputs to the host and runs the oracle on the same bytes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_03_gb300 as msa
+import msa_synth as ms
+from oracle import msa_oracle as O
+
+from _helpers import bind, check_out, check_pooled, check_selection, gpu_path, workspace
+
+pytestmark = pytest.mark.gpu
+
+KV = ["bf16", "fp8", "nvfp4"]
+
+
+def _case(name, **over):
+    w = ms.make_workload(name, **over)
+    c = ms.make_case(w, device="cuda")
+    return w, c, ms.case_to_host(c)
+
+
+# ---------------------------------------------------------------- a1: decode of stored elements
+
+@pytest.mark.parametrize("kv", KV)
+def test_dequant_bit_exact(kv):
+    w, c, h = _case("tiny_bf16", seq_lens=(700, 300), kv_dtype=kv, index_dtype=kv)
+    cache, _, _, _ = bind(c)
+    phys = torch.tensor(list(range(c["num_blocks"])) + [-1, c["num_blocks"]], dtype=torch.int32, device="cuda")
+    n = phys.numel()
+    for which in (0, 1, 2):
+        heads = 1 if which == 2 else w.num_kv_heads
+        out = torch.empty((n, heads, 128, 128), dtype=torch.float32, device="cuda")
+        msa.msa_dequant_debug(cache, which, phys, out)
+        got = out.cpu().numpy()
+        for i in range(c["num_blocks"]):
+            ref = O.dequant_index_tile(h, i)[None] if which == 2 else O.dequant_kv_tile(h, "kv"[which], i)
+            assert np.array_equal(got[i].view(np.uint32), ref.astype(np.float32).view(np.uint32)), (kv, which, i)
+        assert np.isnan(got[-2:]).all()
+
+
+# ---------------------------------------------------------------- a2-a6 staged, a9 fused
+
+STAGED_CASES = [
+    ("tiny_bf16", {}),
+    ("tiny_bf16", dict(topk=32)),
+    ("fp8_decode", dict(seq_lens=(1000, 2500, 3333, 777), seed=11)),
+    ("fp8_decode", dict(seq_lens=(4096, 129, 128, 1), seed=12)),
+    ("nvfp4_verify", dict(seq_lens=(5000, 3000), seed=13)),
+    ("nvfp4_verify", dict(seq_lens=(1029, 1024 + 3), seed=14)),  # 8 verify tokens straddle a block edge
+    ("fp8_long", dict(seq_lens=(20000, 9000), seed=15)),
+    ("fp8_decode", dict(seq_lens=(3000, 2000), q_per_seq=4, seed=16)),  # bf16 q, multi-token FP8
+    ("tiny_bf16", dict(seq_lens=(2000, 1500), kv_dtype="fp8", index_dtype="nvfp4", seed=17)),
+    ("tiny_bf16", dict(seq_lens=(2000,), kv_dtype="nvfp4", index_dtype="bf16", q_dtype="fp8", seed=18)),
+]
+
+
+@pytest.mark.parametrize("name,over", STAGED_CASES)
+def test_staged_path_matches_oracle(name, over):
+    w, c, h = _case(name, **over)
+    g = gpu_path(c, fused=False)
+    ref = O.run_path(h, topk=w.topk)
+    check_pooled(g["pooled"], ref["pooled"])
+    check_selection(g["topk"], ref["pooled"], w.seq_lens, w.q_per_seq, w.topk)
+    out = np.zeros_like(ref["out"])
+    for s in range(w.num_seqs):  # the oracle's attend on the GPU's own selection
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+    check_out(g["out"], out)
+
+
+@pytest.mark.parametrize("name,over", STAGED_CASES[:7])
+def test_fused_decode_matches_staged(name, over):
+    w, c, h = _case(name, **over)
+    a = gpu_path(c, fused=False)
+    b = gpu_path(c, fused=True)
+    assert np.array_equal(a["topk"], b["topk"])
+    assert np.array_equal(a["out"], b["out"])
+    assert np.array_equal(a["lse"], b["lse"])
+
+
+def test_lse_matches_oracle():
+    w, c, h = _case("fp8_decode", seq_lens=(3000, 1111), seed=21)
+    g = gpu_path(c)
+    for s in range(w.num_seqs):
+        o, lse = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        assert np.abs(g["lse"][s] - lse[0]).max() < 1e-3
+
+
+def test_topk32_equals_dense_attention():
+    # with k >= number of blocks the path is dense causal attention
+    w, c, h = _case("tiny_bf16", topk=32)
+    g = gpu_path(c)
+    assert np.array_equal(g["topk"][0, 0], np.arange(32))
+    T = w.seq_lens[0]
+    K = np.concatenate([O.dequant_kv_tile(h, "k", int(h["block_table"][0, b])) for b in range(32)], axis=1)
+    V = np.concatenate([O.dequant_kv_tile(h, "v", int(h["block_table"][0, b])) for b in range(32)], axis=1)
+    q = O.query_values(h["q"], "bf16", 1.0)[0]
+    ref = np.stack([O.attend(q[hh], K[hh // 4, :T], V[hh // 4, :T], 128 ** -0.5)[0] for hh in range(16)])
+    check_out(g["out"][0], ref)
+
+
+@pytest.mark.parametrize("topk", [4, 8, 32])
+def test_other_topk(topk):
+    w, c, h = _case("fp8_decode", seq_lens=(5000, 300), topk=topk, seed=30 + topk)
+    g = gpu_path(c, fused=False)
+    ref = O.run_path(h, topk=topk)
+    check_pooled(g["pooled"], ref["pooled"])
+    check_selection(g["topk"], ref["pooled"], w.seq_lens, 1, topk)
+
+
+def test_init_and_local_blocks():
+    w, c, h = _case("fp8_decode", seq_lens=(6000, 2000), seed=40)
+    cfg = msa.Config(topk=16, init_blocks=2, local_blocks=3)
+    g = gpu_path(c, cfg=cfg, fused=False)
+    ref = O.run_path(h, topk=16, init_blocks=2, local_blocks=3)
+    check_selection(g["topk"], ref["pooled"], w.seq_lens, 1, 16, 2, 3)
+
+
+def test_planted_hot_blocks_selected():
+    w, c, h = _case("fp8_decode", seq_lens=(12000, 9000, 7000), seed=41)
+    g = gpu_path(c)
+    for s in range(w.num_seqs):
+        for grp in range(w.num_kv_heads):
+            assert set(h["hot"][s, grp]).issubset(set(g["topk"][s, grp]))
+
+
+def test_bad_block_table_sets_status_not_trap():
+    w, c, h = _case("fp8_decode", seq_lens=(2000, 2000), seed=42)
+    c["block_table"][1, 3] = c["num_blocks"] + 5
+    cache, batch, iq, q = bind(c)
+    cfg = msa.default_config()
+    ws = workspace(cache, batch, cfg, 16)
+    topk = torch.empty((2, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, 16, topk, out, None, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    assert st == 5 and flags & 1
+    # the context stays usable and the status word was cleared
+    msa.msa_decode(cache, batch, cfg, iq, q, 16, topk, out, None, ws)
+    torch.cuda.synchronize()
+    st2, _ = msa.msa_read_device_status(ws)
+    assert st2 == 5  # still bad data -> flagged again
+
+
+def test_host_errors_launch_nothing():
+    w, c, h = _case("fp8_decode", seq_lens=(2000,), seed=43)
+    cache, batch, iq, q = bind(c)
+    cfg = msa.default_config()
+    ws = workspace(cache, batch, cfg, 16)
+    topk = torch.empty((1, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_decode(cache, batch, msa.Config(topk=12), iq, q, 16, topk, out, None, ws)
+    assert e.value.status == 2
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_decode(cache, batch, cfg, iq, q, 16, topk, out, None, ws[:1000])
+    assert e.value.status == 3
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_decode(cache, batch, cfg, iq, q, 15, topk, out, None, ws)
+    assert e.value.status == 1
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled
+
+@pytest.mark.parametrize("name,seqs", [("tiny_bf16", [0]), ("fp8_decode", [0, 17, 31]),
+                                       ("fp8_long", [2]), ("nvfp4_verify", [5])])
+def test_full_size_sampled(name, seqs):
+    w = ms.make_workload(name)
+    c = ms.make_case(w, device="cuda")
+    g = gpu_path(c)
+    h = ms.case_to_host(c)
+    del c
+    torch.cuda.empty_cache()
+    Q = w.q_per_seq
+    for s in seqs:
+        pooled = O.pooled_scores(h, s, w.index_dim ** -0.5)
+        rows = list(range(s * Q, (s + 1) * Q))
+        full = np.full((w.num_seqs * Q, w.num_kv_heads, w.max_blocks), -np.inf)
+        full[rows] = pooled
+        check_selection(g["topk"], full, w.seq_lens, Q, w.topk, rows=rows)
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        check_out(g["out"][rows], o)
