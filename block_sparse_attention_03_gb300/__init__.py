@@ -27,7 +27,7 @@ DTYPES = {"bf16": 0, "fp8": 1, "nvfp4": 2}
 # every symbol include/msa.h declares
 EXPORTS = ("msa_workspace_size", "msa_workspace_init", "msa_indexer_score", "msa_topk_blocks",
            "msa_sparse_attend", "msa_decode", "msa_read_device_status", "msa_status_string",
-           "msa_dequant_debug")
+           "msa_dequant_debug", "msa_decode_noalloc")
 
 
 class MsaError(RuntimeError):
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
         h.msa_status_string.restype = ctypes.c_char_p
         h.msa_status_string.argtypes = [ctypes.c_int]
         h.msa_dequant_debug.argtypes = [P, ctypes.c_int32, P, ctypes.c_int32, P, P]
+        h.msa_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_int32, P, P, P, P, P]
         for name in EXPORTS:
             if name != "msa_workspace_size" and name != "msa_status_string":
                 getattr(h, name).restype = ctypes.c_int
@@ -241,6 +242,20 @@ def msa_dequant_debug(cache, which: int, phys_blocks, out, stream=None) -> None:
                                    _stream(stream)), "msa_dequant_debug")
 
 
+def msa_decode_noalloc(cache, batch, cfg, index_q: Query, q: Query, num_q_heads: int, topk_idx, out, lse,
+                       status_out=None, stream=None) -> None:
+    """msa_decode without a caller workspace, for callers that cannot allocate
+    device memory (e.g. code living inside another framework's memory pool):
+    the library's own fixed scratch array is used instead.  Problems whose
+    workspace exceeds the scratch size are rejected; calls must not overlap on
+    the GPU because they share that scratch.  status_out: optional device
+    int32[2] that receives the call's device status flags."""
+    c, b, f, iq, qq = cache.struct(), batch.struct(), cfg.struct(), index_q.struct(), q.struct()
+    _check(lib().msa_decode_noalloc(_ref(c), _ref(b), _ref(f), _ref(iq), _ref(qq), num_q_heads, _ptr(topk_idx),
+                                    _ptr(out), _ptr(lse), _ptr(status_out), _stream(stream)),
+           "msa_decode_noalloc")
+
+
 def default_config(topk: int = 16, head_dim: int = 128, index_dim: int = 128) -> Config:
     """The model's settings: index and softmax scales head_dim ** -0.5."""
     return Config(topk=topk, index_scale=index_dim ** -0.5, sm_scale=head_dim ** -0.5)
@@ -249,4 +264,4 @@ def default_config(topk: int = 16, head_dim: int = 128, index_dim: int = 128) ->
 __all__ = ["PagedCache", "Batch", "Config", "Query", "MsaError", "lib", "EXPORTS", "default_config",
            "msa_workspace_size", "msa_workspace_init", "msa_indexer_score", "msa_topk_blocks",
            "msa_sparse_attend", "msa_decode", "msa_read_device_status", "msa_status_string",
-           "msa_dequant_debug", "roofline"]
+           "msa_dequant_debug", "msa_decode_noalloc", "roofline"]

@@ -449,3 +449,69 @@ msa_status_t msa_dequant_debug(const msa_cache_t* cache, int32_t which, const in
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free decode
+//
+// Some callers cannot allocate device memory for a workspace: code that runs
+// inside another framework's memory pool or allocator hooks, a plugin that
+// must not call cudaMalloc (or torch's allocator) on its hot path, or a
+// process whose device memory is fully reserved up front.  msa_decode_noalloc
+// serves them with a fixed scratch area that lives in the library itself: the
+// array below is part of the library's device image, so every GPU that loads
+// libmsa holds these bytes until the process exits.
+
+// MSA_NOALLOC_SCRATCH_BYTES (include/msa.h): the largest workspace it accepts.
+static __device__ __align__(256) unsigned char msa_noalloc_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of msa_noalloc_scratch on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+msa_status_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64];
+  static bool have[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, msa_noalloc_scratch) != cudaSuccess || p == nullptr) return MSA_ERR_CUDA;
+    addr[dev] = p;
+    have[dev] = true;
+  }
+  *out = addr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_batch_t* batch,
+                                           const msa_config_t* cfg, const msa_query_t* index_q,
+                                           const msa_query_t* q, int32_t num_q_heads, int32_t* topk_idx,
+                                           void* out, float* lse, int32_t* status_out, msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK || (s = check_cache(cache, true, true)) != MSA_OK ||
+      (s = check_query(index_q)) != MSA_OK || (s = check_query(q)) != MSA_OK)
+    return s;
+  if (!topk_idx || !out || !aligned16(out)) return MSA_ERR_INVALID_ARGUMENT;
+  Plan pl;
+  if ((s = make_plan(cache, batch, cfg, num_q_heads, index_q->dtype == MSA_DTYPE_FP8_E4M3,
+                     q->dtype == MSA_DTYPE_FP8_E4M3, pl)) != MSA_OK)
+    return s;
+  if (pl.total > MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  if ((s = noalloc_scratch(&ws)) != MSA_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the status word must start at zero; every other region is written before it is read
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MSA_ERR_CUDA;
+  float* pooled = at<float>(ws, pl.off_pooled);
+  if ((s = run_indexer(cache, batch, cfg, index_q, pl, ws, pooled, st)) != MSA_OK) return s;
+  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true)) != MSA_OK)
+    return s;
+  if ((s = run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st, false)) != MSA_OK) return s;
+  if (status_out &&
+      cudaMemcpyAsync(status_out, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  return MSA_OK;
+}

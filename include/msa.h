@@ -214,6 +214,31 @@ msa_status_t msa_dequant_debug(const msa_cache_t* cache, int32_t which,
                                const int32_t* phys_blocks, int32_t n, float* out,
                                msa_stream_t stream);
 
+/* Allocation-free variant of msa_decode (no counterpart in the paper; a
+ * deployment convenience).  Some callers cannot allocate device memory for a
+ * workspace: code running inside another framework's memory pool, a plugin
+ * that must not call cudaMalloc (or a framework allocator) on its hot path, a
+ * process whose device memory is reserved up front.  This entry point uses a
+ * fixed scratch array inside the library instead of a caller workspace; it
+ * allocates nothing and calls no allocating routine.
+ *   - Limit: the problem's msa_workspace_size must be at most
+ *     MSA_NOALLOC_SCRATCH_BYTES (8 MiB, held on every GPU that loads the
+ *     library until the process exits); larger problems return
+ *     MSA_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *   - The first call on each device looks up the scratch's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents; each call clears what must start at zero.  Calls that overlap
+ *     on the GPU (other streams, other host threads) race on it: serialise them.
+ *   - status_out: optional device int32[2]; receives this call's device status
+ *     flags (the same bits msa_read_device_status reports) at the end of the call.
+ * Arguments, outputs and errors are otherwise those of msa_decode. */
+#define MSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_batch_t* batch,
+                                const msa_config_t* cfg, const msa_query_t* index_q,
+                                const msa_query_t* q, int32_t num_q_heads, int32_t* topk_idx,
+                                void* out, float* lse, int32_t* status_out, msa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

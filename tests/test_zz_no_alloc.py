@@ -1,0 +1,80 @@
+"""The allocation-free decode entry point, for callers that cannot allocate
+device memory (code inside another framework's memory pool, plugins that may
+not call cudaMalloc on their hot path).  It runs the same kernels as
+msa_decode on a fixed scratch array inside the library, so its results must
+match msa_decode's; two calls in a row check that the shared scratch carries
+nothing stale from one call into the next.  This file is collected last."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_03_gb300 as msa
+import msa_synth as ms
+
+from _helpers import OUT_MAX_ABS, OUT_MEAN_ABS, bind, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_sparse_attention_03_gb300 import _build
+    _build.build()
+
+
+def _with_workspace(case):
+    w = case["workload"]
+    cache, batch, iq, q = bind(case)
+    cfg = msa.default_config(w.topk)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    rows = w.num_seqs * w.q_per_seq
+    topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device="cuda")
+    out = torch.empty((rows, w.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((rows, w.num_q_heads), dtype=torch.float32, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, lse, ws)
+    assert msa.msa_read_device_status(ws)[0] == 0
+    return topk.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _without_workspace(case):
+    w = case["workload"]
+    cache, batch, iq, q = bind(case)
+    cfg = msa.default_config(w.topk)
+    rows = w.num_seqs * w.q_per_seq
+    topk = torch.full((rows, w.num_kv_heads, w.topk), -5, dtype=torch.int32, device="cuda")
+    out = torch.full((rows, w.num_q_heads, 128), 9.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((rows, w.num_q_heads), dtype=torch.float32, device="cuda")
+    status = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    msa.msa_decode_noalloc(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, lse, status)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    return topk.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def test_noalloc_matches_decode_on_two_calls_in_a_row():
+    # two different problems back to back through the same scratch
+    cases = [ms.make_case(ms.make_workload("fp8_decode", seq_lens=(9000, 3000, 700), seed=91), device="cuda"),
+             ms.make_case(ms.make_workload("nvfp4_verify", seq_lens=(4000, 2100), seed=92), device="cuda")]
+    for case in cases:
+        t_ref, o_ref, l_ref = _with_workspace(case)
+        t, o, l = _without_workspace(case)
+        assert np.array_equal(t, t_ref)
+        err = np.abs(o - o_ref)
+        assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS
+        assert np.abs(l - l_ref).max() <= 1e-3
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch():
+    w = ms.make_workload("fp8_decode", seq_lens=(1000,) * 24, q_per_seq=8, seed=93)
+    case = ms.make_case(w, device="cuda")
+    cache, batch, iq, q = bind(case)
+    cfg = msa.default_config()
+    assert msa.msa_workspace_size(cache, batch, cfg, 16) > 8 << 20
+    topk = torch.empty((24 * 8, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((24 * 8, 16, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_decode_noalloc(cache, batch, cfg, iq, q, 16, topk, out, None)
+    assert e.value.status == 3
