@@ -31,8 +31,13 @@ WORKLOAD_TEXT = {
                 "dim 128, top-16, FP8 E4M3 K/V/index keys + per-token scales, bf16 queries",
     "nvfp4_verify": "NVFP4 speculative verify: 8 seqs x 128K, 8 query tokens each, NVFP4 K/V/index keys, E4M3 queries",
     "tiny_bf16": "Tiny BF16 decode: 1 seq x 4096 tokens, 1 query, BF16 everything",
+    "fp8_prefill": "Prefill chunk: 8192 new tokens on a 64K-token FP8 E4M3 context (1 seq), bf16 queries, "
+                   "per-query top-16, causal",
 }
-KERNELS_PER_STEP = 7  # prep(index q), indexer, top-k, prep(q), union, attend, combine
+
+def kernels_per_step(q_per_seq: int) -> int:
+    """Launches of one msa_decode: indexer, top-k, (union when several query tokens), attend."""
+    return 3 if q_per_seq == 1 else 4
 
 
 def parse():
@@ -47,12 +52,22 @@ def parse():
 
 
 def load_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, kind) from the driver's measurement, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def indexer_flops(w):
+    """Algorithmic FLOPs of the index scores: every visible key x groups x index dim x 2."""
+    tot = 0
+    for T in w.seq_lens:
+        first = T - w.q_per_seq + 1  # keys visible to the first new token
+        tot += w.q_per_seq * first + w.q_per_seq * (w.q_per_seq - 1) // 2
+    return 2.0 * tot * w.num_kv_heads * w.index_dim
 
 
 class ClockSampler:
@@ -110,6 +125,20 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank runs its own, independent replica of the workload."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(values, world: int, dist=None, device=None):
+    """Element-wise max of per-rank timings (the slowest rank defines the step)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
 
 
 def algorithmic_bytes(w, sel_union_blocks):
@@ -194,7 +223,7 @@ def main():
     import msa_synth as ms
 
     base = ms.make_workload(args.workload)
-    w = ms.make_workload(args.workload, seed=base.seed + 1000 * rank)
+    w = ms.make_workload(args.workload, seed=replica_seed(base.seed, rank))
     case = ms.make_case(w, device=dev)
     cache = msa.PagedCache(kv_dtype=w.kv_dtype, index_dtype=w.index_dtype, num_blocks=case["num_blocks"],
                            num_kv_heads=w.num_kv_heads, k=case["k"], v=case["v"], idx=case["idx"],
@@ -212,8 +241,16 @@ def main():
     topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device=dev)
     out = torch.empty((rows, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((rows, w.num_q_heads), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    # L2 flush between timed steps: write 256 MB (> 129 MB L2), then read 512 MB so
+    # that the written lines are already back in HBM and L2 holds only clean data
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
 
     def step():
         msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, lse, ws, stream)
@@ -234,7 +271,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
@@ -250,7 +287,7 @@ def main():
     for _ in range(3):
         msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws, stream)
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         ievs[i][0].record(stream)
         msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws, stream)
         ievs[i][1].record(stream)
@@ -270,7 +307,7 @@ def main():
     e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         e2e_evs[i][0].record(stream)
         case["index_q"].copy_(h_iq, non_blocking=True)
         case["q"].copy_(h_q, non_blocking=True)
@@ -299,13 +336,10 @@ def main():
         unions.append(per_g)
     idx_bytes, kv_bytes, actual_bytes = algorithmic_bytes(w, unions)
     step_bytes = idx_bytes + kv_bytes
-    peak, peak_kind = load_peaks()
+    peak, bf16_tflops, peak_kind = load_peaks()
 
     # max over ranks
-    vals = torch.tensor([ms_step, idx_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_step, idx_ms, e2e_ms = (float(x) for x in vals.cpu())
+    ms_step, idx_ms, e2e_ms = max_over_ranks([ms_step, idx_ms, e2e_ms], world, dist, dev)
     queries = rows * world
     qps = queries / (ms_step * 1e-3)
     e2e_qps = queries / (e2e_ms * 1e-3)
@@ -333,17 +367,23 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 MMA, fp32 accumulate" if w.kv_dtype == "fp8" else w.kv_dtype,
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed (256 MB write) before every timed step",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed before every timed step (256 MB write, then 512 MB read)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "path_hbm_gbs": path_gbs, "path_frac_of_peak": path_gbs / peak,
             "bytes_per_step": {"algorithmic": step_bytes, "index": idx_bytes, "kv_selected": kv_bytes,
                                "with_fp32_scales": actual_bytes},
-            "roofline": {"bound": "hbm", "kernel": "indexer (prep + score/pool launch)", "achieved": idx_gbs,
-                         "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
-                         "peak_kind": peak_kind},
+            "roofline": ({"bound": "hbm", "kernel": "indexer_kernel (score + block max-pool)", "achieved": idx_gbs,
+                          "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                          "peak_kind": peak_kind} if w.q_per_seq <= 8 else
+                         {"bound": "tensor", "kernel": "indexer_kernel (score + block max-pool)",
+                          "achieved": indexer_flops(w) / (idx_ms * 1e-3) / 1e12,
+                          "peak": 2.0 * bf16_tflops, "unit": "TFLOP/s",
+                          "frac": indexer_flops(w) / (idx_ms * 1e-3) / 1e12 / (2.0 * bf16_tflops),
+                          "traffic": None,
+                          "peak_kind": peak_kind + " (bf16 burst x 2 for e4m3, the nominal ratio)"}),
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": kernels_per_step(w.q_per_seq) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

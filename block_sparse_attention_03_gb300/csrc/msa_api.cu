@@ -82,7 +82,7 @@ msa_status_t check_batch(const msa_batch_t* b) {
   if (!b || !b->seq_lens || !b->block_table) return MSA_ERR_INVALID_ARGUMENT;
   if (b->num_seqs < 1 || b->q_per_seq < 1 || b->max_blocks_per_seq < 1) return MSA_ERR_INVALID_ARGUMENT;
   if ((long)b->max_blocks_per_seq * kBlock > (1l << 30)) return MSA_ERR_UNSUPPORTED;
-  if (b->q_per_seq > 32) return MSA_ERR_UNSUPPORTED;  // decode / verify path: up to 32 new tokens
+  if ((long)b->q_per_seq > (long)b->max_blocks_per_seq * kBlock) return MSA_ERR_INVALID_ARGUMENT;
   return MSA_OK;
 }
 
@@ -140,10 +140,13 @@ FragGeom geom_for(int key_fmt, bool q_fp8, int cols) {
 }
 
 struct Plan {
+  int S = 0, Q = 0, chunks = 1;  // sequences / query tokens as the kernels see them (long chunks split)
   FragGeom gi, ga;          // indexer / attend query geometry
   int bps = 0, splits = 0, cap = 0, r = 0;
-  size_t off_status = 0, off_qfi = 0, off_cfi = 0, off_qfa = 0, off_cfa = 0, off_pooled = 0, off_uids = 0,
-         off_umask = 0, off_ucount = 0, off_po = 0, off_pml = 0, total = 0;
+  bool direct = false;      // one query token: the attend reads the selection rows directly
+  size_t off_status = 0, off_pooled = 0, off_uids = 0, off_umask = 0, off_ucount = 0, off_ctr = 0, off_qfa = 0,
+         off_cfa = 0, off_po = 0, off_pml = 0, total = 0;
+  int nctr = 0;             // attend counters: [S*G] per (sequence, group) + 1 unit counter
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -151,7 +154,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Plan for the given problem.  iq_fp8 / q_fp8: query dtypes (E4M3 or bf16).
 msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, int hq, bool iq_fp8,
                        bool q_fp8, Plan& pl) {
-  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+  // more than 8 new tokens per sequence (a prefill chunk): split into virtual
+  // sequences of the largest of 8, 4, 2, 1 tokens dividing the count
+  int QV = b->q_per_seq;
+  if (QV > 8) {
+    QV = 8;
+    while (b->q_per_seq % QV) QV >>= 1;
+  }
+  pl.chunks = b->q_per_seq / QV;
+  pl.S = b->num_seqs * pl.chunks;
+  pl.Q = QV;
+  const int S = pl.S, Q = pl.Q, G = c->num_kv_heads;
   if (hq < G || hq % G != 0) return MSA_ERR_INVALID_ARGUMENT;
   pl.r = hq / G;
   const int fi = fmt_of(c->index_dtype), fa = fmt_of(c->kv_dtype);
@@ -159,19 +172,23 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.ga = geom_for(fa < 0 ? FMT_FP8 : fa, q_fp8, Q * pl.r);
   if (pl.gi.nt > kMaxIndexerNT || pl.gi.nt * pl.gi.sp > 8) return MSA_ERR_UNSUPPORTED;
   if (pl.ga.cols > kMaxAttendCols || pl.ga.nt * pl.ga.sp > 8) return MSA_ERR_UNSUPPORTED;
-  pl.bps = attend_max_stages(fa < 0 ? FMT_FP8 : fa);
   pl.cap = Q * cfg->topk;
+  pl.direct = (b->q_per_seq == 1);
+  // blocks per split: about two units per SM, at most 4
+  const long items = (long)S * G * pl.cap;
+  const long per = (items + 2l * sm_count() - 1) / (2l * sm_count());
+  pl.bps = (int)(per < 1 ? 1 : (per > 4 ? 4 : per));
   pl.splits = (pl.cap + pl.bps - 1) / pl.bps;
+  pl.nctr = S * G + 1;
   size_t o = 0;
   pl.off_status = o; o = align256(o + 256);
-  pl.off_qfi = o; o = align256(o + (size_t)S * pl.gi.words_per_unit() * 4);
-  pl.off_cfi = o; o = align256(o + (size_t)S * pl.gi.nt * 8 * 4);
-  pl.off_qfa = o; o = align256(o + (size_t)S * G * pl.ga.words_per_unit() * 4);
-  pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
   pl.off_pooled = o; o = align256(o + (size_t)S * Q * G * b->max_blocks_per_seq * 4);
   pl.off_uids = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_umask = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_ucount = o; o = align256(o + (size_t)S * G * 4);
+  pl.off_ctr = o; o = align256(o + (size_t)pl.nctr * 4);
+  pl.off_qfa = o; o = align256(o + (size_t)S * G * pl.ga.words_per_unit() * 4);
+  pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
   pl.off_po = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 128 * 4);
   pl.off_pml = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 2 * 4);
   pl.total = o;
@@ -183,13 +200,15 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-BatchDev batch_dev(const msa_batch_t* b) {
+BatchDev batch_dev(const msa_batch_t* b, const Plan& pl) {
   BatchDev d;
   d.seq_lens = b->seq_lens;
   d.block_table = b->block_table;
-  d.S = b->num_seqs;
-  d.Q = b->q_per_seq;
+  d.S = pl.S;
+  d.Q = pl.Q;
   d.max_nb = b->max_blocks_per_seq;
+  d.chunks = pl.chunks;
+  d.q_real = b->q_per_seq;
   return d;
 }
 
@@ -199,20 +218,8 @@ msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA
 
 msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* iq,
                          const Plan& pl, void* ws, float* pooled, cudaStream_t st) {
-  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+  const int G = c->num_kv_heads;
   const int fi = fmt_of(c->index_dtype);
-  PrepParams pp;
-  pp.q = iq->data;
-  pp.q_is_fp8 = iq->dtype == MSA_DTYPE_FP8_E4M3;
-  pp.q_scale = pp.q_is_fp8 ? iq->scale : 1.f;
-  pp.col_const = cfg->index_scale * (fi == FMT_NVFP4 ? c->idx_global : 1.f);
-  pp.key_fmt = fi;
-  pp.geom = pl.gi;
-  pp.units = S;
-  pp.frag = at<uint32_t>(ws, pl.off_qfi);
-  pp.colf = at<float>(ws, pl.off_cfi);
-  cudaError_t e = launch_prep_rows(pp, Q * G, 1, 0, G, G, st);
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
   CUtensorMap tm;
   const CUtensorMap* tmp = nullptr;
   if (fi != FMT_NVFP4) {
@@ -220,24 +227,57 @@ msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_c
     tmp = &tm;
   }
   IndexerParams ip;
-  ip.batch = batch_dev(b);
+  ip.batch = batch_dev(b, pl);
   ip.G = G;
   ip.num_blocks = c->num_blocks;
   ip.idx = static_cast<const uint8_t*>(c->idx);
   ip.idx_sf = static_cast<const uint8_t*>(c->idx_sf);
   ip.idx_scale = c->idx_scale;
-  ip.qfrag = pp.frag;
-  ip.colf = pp.colf;
+  ip.index_q = iq->data;
+  ip.iq_fp8 = iq->dtype == MSA_DTYPE_FP8_E4M3;
+  ip.iq_scale = ip.iq_fp8 ? iq->scale : 1.f;
+  ip.col_const = cfg->index_scale * (fi == FMT_NVFP4 ? c->idx_global : 1.f);
   ip.geom = pl.gi;
   ip.pooled = pooled;
   ip.status = at<DeviceStatus>(ws, pl.off_status);
-  return cuda_status(launch_indexer(fi, tmp, ip, sm_count(), st, true));
+  // first kernel of the call: plain stream order, so every earlier write to the
+  // caches and queries is complete and visible before it reads them
+  return cuda_status(launch_indexer(fi, tmp, ip, sm_count(), st, false));
 }
 
+// fill the attend query-fragment job of a top-k / union launch
+template <typename P>
+void set_frag_job(P& kp, const msa_cache_t* c, const msa_config_t* cfg, const msa_query_t* q, int hq, const Plan& pl,
+                  void* ws) {
+  const int fa = fmt_of(c->kv_dtype);
+  kp.q = q->data;
+  kp.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
+  kp.q_scale = kp.q_fp8 ? q->scale : 1.f;
+  kp.col_const = cfg->sm_scale * 1.4426950408889634f * (fa == FMT_NVFP4 ? c->k_global : 1.f);
+  kp.key_fmt = fa;
+  kp.r = pl.r;
+  kp.hq = hq;
+  kp.geom = pl.ga;
+  kp.frag = at<uint32_t>(ws, pl.off_qfa);
+  kp.colf = at<float>(ws, pl.off_cfa);
+}
+
+struct FragJob {
+  const msa_cache_t* c;
+  const msa_query_t* q;
+  int hq;
+};
+
 msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, const float* pooled, int32_t* topk_idx,
-                      float* topk_score, void* ws, const Plan* pl, cudaStream_t st, bool pdl) {
+                      float* topk_score, void* ws, const Plan* pl, cudaStream_t st, bool pdl, bool clear_ctr,
+                      const FragJob* frag_job = nullptr) {
   TopkParams tp;
-  tp.batch = batch_dev(b);
+  // positions T - Q + i are the same with or without virtual sequences: the real batch
+  Plan real;
+  real.S = b->num_seqs;
+  real.Q = b->q_per_seq;
+  real.chunks = 1;
+  tp.batch = batch_dev(b, real);
   tp.G = G;
   tp.topk = cfg->topk;
   tp.init_blocks = cfg->init_blocks;
@@ -246,30 +286,26 @@ msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, cons
   tp.topk_idx = topk_idx;
   tp.topk_score = topk_score;
   tp.status = pl ? at<DeviceStatus>(ws, pl->off_status) : static_cast<DeviceStatus*>(ws);
+  tp.zero = (pl && clear_ctr) ? at<int32_t>(ws, pl->off_ctr) : nullptr;
+  tp.nzero = (pl && clear_ctr) ? pl->nctr : 0;
+  tp.frag = nullptr;
+  tp.colf = nullptr;
+  if (frag_job && pl) set_frag_job(tp, frag_job->c, cfg, frag_job->q, frag_job->hq, *pl, ws);
   return cuda_status(launch_topk(tp, st, pdl));
 }
 
 msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* q,
                         int hq, const int32_t* topk_idx, void* out, float* lse, const Plan& pl, void* ws,
-                        cudaStream_t st, bool prep_done) {
-  const int S = b->num_seqs, Q = b->q_per_seq, G = c->num_kv_heads;
+                        cudaStream_t st, bool prepared) {
+  // prepared: the preceding top-k launch (one query token) already cleared the
+  // counters and wrote the query fragments; otherwise the union kernel does both
+  const int G = c->num_kv_heads;
   const int fa = fmt_of(c->kv_dtype);
   DeviceStatus* status = at<DeviceStatus>(ws, pl.off_status);
-  if (!prep_done) {
-    PrepParams pp;
-    pp.q = q->data;
-    pp.q_is_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
-    pp.q_scale = pp.q_is_fp8 ? q->scale : 1.f;
-    pp.col_const = cfg->sm_scale * 1.4426950408889634f * (fa == FMT_NVFP4 ? c->k_global : 1.f);
-    pp.key_fmt = fa;
-    pp.geom = pl.ga;
-    pp.units = S * G;
-    pp.frag = at<uint32_t>(ws, pl.off_qfa);
-    pp.colf = at<float>(ws, pl.off_cfa);
-    if (launch_prep_rows(pp, Q * hq, G, pl.r, pl.r, hq, st) != cudaSuccess) return MSA_ERR_CUDA;
-  }
+  int32_t* ctr = at<int32_t>(ws, pl.off_ctr);
+  const bool direct = prepared && pl.direct;
   UnionParams up;
-  up.batch = batch_dev(b);
+  up.batch = batch_dev(b, pl);
   up.G = G;
   up.topk = cfg->topk;
   up.topk_idx = topk_idx;
@@ -277,8 +313,13 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   up.u_ids = at<int32_t>(ws, pl.off_uids);
   up.u_mask = at<uint32_t>(ws, pl.off_umask);
   up.u_count = at<int32_t>(ws, pl.off_ucount);
+  up.zero = ctr;
+  up.nzero = pl.nctr;
+  set_frag_job(up, c, cfg, q, hq, pl, ws);
   up.status = status;
-  if (launch_union(up, st, true) != cudaSuccess) return MSA_ERR_CUDA;
+  if (!direct) {
+    if (launch_union(up, st, true) != cudaSuccess) return MSA_ERR_CUDA;
+  }
 
   CUtensorMap tk, tv;
   const CUtensorMap *tkp = nullptr, *tvp = nullptr;
@@ -290,7 +331,7 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
     tvp = &tv;
   }
   AttendParams ap;
-  ap.batch = batch_dev(b);
+  ap.batch = batch_dev(b, pl);
   ap.G = G;
   ap.r = pl.r;
   ap.num_blocks = c->num_blocks;
@@ -301,32 +342,30 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   ap.k_scale = c->k_scale;
   ap.v_scale = c->v_scale;
   ap.v_global = c->v_global;
-  ap.qfrag = at<uint32_t>(ws, pl.off_qfa);
-  ap.colf = at<float>(ws, pl.off_cfa);
+  ap.q = q->data;
+  ap.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
+  ap.q_scale = ap.q_fp8 ? q->scale : 1.f;
+  ap.col_const = cfg->sm_scale * 1.4426950408889634f * (fa == FMT_NVFP4 ? c->k_global : 1.f);
   ap.geom = pl.ga;
+  ap.direct = direct ? 1 : 0;
+  ap.frag = up.frag;
+  ap.colf = up.colf;
+  ap.topk_idx = topk_idx;
+  ap.topk = cfg->topk;
   ap.u_ids = up.u_ids;
   ap.u_mask = up.u_mask;
   ap.u_count = up.u_count;
   ap.cap = pl.cap;
   ap.bps = pl.bps;
   ap.splits = pl.splits;
+  ap.work_ctr = ctr + (pl.nctr - 1);
+  ap.sg_ctr = ctr;
   ap.part_o = at<float>(ws, pl.off_po);
   ap.part_ml = at<float>(ws, pl.off_pml);
+  ap.out = out;
+  ap.lse = lse;
   ap.status = status;
-  if (launch_attend(fa, tkp, tvp, ap, st, true) != cudaSuccess) return MSA_ERR_CUDA;
-
-  CombineParams cp;
-  cp.S = S;
-  cp.Q = Q;
-  cp.G = G;
-  cp.r = pl.r;
-  cp.splits = pl.splits;
-  cp.cols = pl.ga.cols;
-  cp.part_o = ap.part_o;
-  cp.part_ml = ap.part_ml;
-  cp.out = out;
-  cp.lse = lse;
-  return cuda_status(launch_combine(cp, st, true));
+  return cuda_status(launch_attend(fa, tkp, tvp, ap, sm_count(), st, true));
 }
 
 }  // namespace
@@ -387,7 +426,8 @@ msa_status_t msa_topk_blocks(const msa_batch_t* batch, const msa_config_t* cfg, 
   if ((s = check_batch(batch)) != MSA_OK || (s = check_cfg(cfg)) != MSA_OK) return s;
   if (num_groups < 1 || num_groups > 8 || !pooled || !topk_idx || !workspace) return MSA_ERR_INVALID_ARGUMENT;
   if (workspace_bytes < 256) return MSA_ERR_WORKSPACE_TOO_SMALL;
-  return run_topk(batch, cfg, num_groups, pooled, topk_idx, topk_score, workspace, nullptr, (cudaStream_t)stream, false);
+  return run_topk(batch, cfg, num_groups, pooled, topk_idx, topk_score, workspace, nullptr, (cudaStream_t)stream, false,
+                  false);
 }
 
 msa_status_t msa_sparse_attend(const msa_cache_t* cache, const msa_batch_t* batch, const msa_config_t* cfg,
@@ -420,9 +460,11 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, cons
   cudaStream_t st = (cudaStream_t)stream;
   float* pooled = at<float>(workspace, pl.off_pooled);
   if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st)) != MSA_OK) return s;
-  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true)) != MSA_OK)
+  const FragJob fj = {cache, q, num_q_heads};
+  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, true,
+                    pl.direct ? &fj : nullptr)) != MSA_OK)
     return s;
-  return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st, false);
+  return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st, true);
 }
 
 msa_status_t msa_read_device_status(void* workspace, msa_stream_t stream, int32_t* detail) {
@@ -507,9 +549,11 @@ extern "C" msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_b
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MSA_ERR_CUDA;
   float* pooled = at<float>(ws, pl.off_pooled);
   if ((s = run_indexer(cache, batch, cfg, index_q, pl, ws, pooled, st)) != MSA_OK) return s;
-  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true)) != MSA_OK)
+  const FragJob fj = {cache, q, num_q_heads};
+  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, true,
+                    pl.direct ? &fj : nullptr)) != MSA_OK)
     return s;
-  if ((s = run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st, false)) != MSA_OK) return s;
+  if ((s = run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st, true)) != MSA_OK) return s;
   if (status_out &&
       cudaMemcpyAsync(status_out, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return MSA_ERR_CUDA;

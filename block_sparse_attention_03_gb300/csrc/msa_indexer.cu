@@ -11,8 +11,9 @@
 // 4 groups x 128 dims it needs 4 MACs per byte, more than the FP32 pipe can
 // issue at HBM rate, so the dot products run on the tensor pipe:
 //   S^T[key][col] = Keys[128 x 128] * Q^T[128 x cols]   (mma.sync, keys = rows)
-// Each warp owns a private ring of NST shared-memory stages; lane 0 streams
-// whole 128-token blocks into it (TMA tensor copy with the 128-byte swizzle
+// Each warp owns a private ring of NST shared-memory stages (several CTAs per
+// SM, so 12 warps per SM hide the copy latency); lane 0 streams whole
+// 128-token blocks into it (TMA tensor copy with the 128-byte swizzle
 // for FP8/BF16, so ldmatrix reads are bank-conflict free; a 1-D bulk copy for
 // NVFP4, whose 64-byte rows are read conflict-free as they are).  Keys are fed
 // to the MMA without conversion (e4m3 / bf16) or dequantized exactly to f16 in
@@ -26,6 +27,7 @@
 // the batch; units past a sequence's end write -inf.
 #include "msa_device.cuh"
 #include "msa_internal.h"
+#include "msa_qfrag.cuh"
 
 namespace msa {
 
@@ -39,21 +41,21 @@ struct IdxTraits<FMT_FP8> {
   static constexpr int KS = 4;               // k32 steps
   static constexpr int TILE = 128 * 128;     // bytes of one block of keys
   static constexpr int SCALES = 128 * 4;     // fp32 per-token scales
-  static constexpr int WARPS = 4, NST = 3;
+  static constexpr int WARPS = 4, NST = 1;   // 3 CTAs (12 warps) per SM
 };
 template <>
 struct IdxTraits<FMT_BF16> {
   static constexpr int KS = 8;
   static constexpr int TILE = 128 * 256;     // two swizzled 128-byte halves
   static constexpr int SCALES = 0;
-  static constexpr int WARPS = 2, NST = 2;
+  static constexpr int WARPS = 4, NST = 1;
 };
 template <>
 struct IdxTraits<FMT_NVFP4> {
   static constexpr int KS = 8;
   static constexpr int TILE = 128 * 64;      // packed e2m1
   static constexpr int SCALES = 128 * 8;     // e4m3 block scales
-  static constexpr int WARPS = 4, NST = 4;
+  static constexpr int WARPS = 4, NST = 2;   // 3 CTAs (12 warps) per SM
 };
 
 // Shared-memory layout of one CTA: per warp NST tiles, NST scale buffers,
@@ -77,108 +79,153 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
   return base + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+// m-tiles computed together: bounds the accumulator registers to 32 per lane
+// while keeping enough independent MMA chains in flight.
+template <int NT>
+__host__ __device__ constexpr int m_group() {
+  return NT >= 8 ? 1 : 8 / NT;
+}
+
+// Score one 128-key block held in shared memory: per lane, the running max
+// over its rows of each of its columns (2 per 8-wide tile).
 template <int FMT, int NT, int SP>
-__device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* scales, const uint32_t (&bq)[SP][NT][IdxTraits<FMT>::KS][2],
-                                            int lane, int key0, const int lim_col[NT][2], float (&cmax)[NT][2]) {
+__device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* scales,
+                                            const uint32_t (&bq)[SP][NT][IdxTraits<FMT>::KS][2], int lane, int key0,
+                                            const int (&lim)[NT][2], float (&cmax)[NT][2]) {
   constexpr int KS = IdxTraits<FMT>::KS;
+  constexpr int MG = m_group<NT>();
   const int g = lane >> 2, j = lane & 3;
   const uint32_t tb = smem_u32(tile);
 #pragma unroll 1
-  for (int m = 0; m < 8; ++m) {
-    float acc[NT][4];
+  for (int m0 = 0; m0 < 8; m0 += MG) {
+    float acc[MG][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int mi = 0; mi < MG; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[mi][nt][0] = acc[mi][nt][1] = acc[mi][nt][2] = acc[mi][nt][3] = 0.f;
     if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
-      const int row = 16 * m + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a[4];
-        if constexpr (FMT == FMT_FP8) {
-          ldmatrix_x4(a, swz(tb, row, 2 * ks + (lane >> 4)));
+        uint32_t a[MG][4];
 #pragma unroll
-          for (int sp = 0; sp < SP; ++sp)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_e4m3_k32(acc[nt], a, bq[sp][nt][ks][0], bq[sp][nt][ks][1]);
-        } else {
-          const uint32_t half = tb + (ks >> 2) * (128 * 128);
-          ldmatrix_x4(a, swz(half, row, 2 * (ks & 3) + (lane >> 4)));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_k16(acc[nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+        for (int mi = 0; mi < MG; ++mi) {
+          const int row = 16 * (m0 + mi) + (lane & 7) + ((lane >> 3) & 1) * 8;
+          if constexpr (FMT == FMT_FP8)
+            ldmatrix_x4(a[mi], swz(tb, row, 2 * ks + (lane >> 4)));
+          else
+            ldmatrix_x4(a[mi], swz(tb + (ks >> 2) * (128 * 128), row, 2 * (ks & 3) + (lane >> 4)));
         }
+#pragma unroll
+        for (int sp = 0; sp < SP; ++sp)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int mi = 0; mi < MG; ++mi) {
+              if constexpr (FMT == FMT_FP8)
+                mma_e4m3_k32(acc[mi][nt], a[mi], bq[sp][nt][ks][0], bq[sp][nt][ks][1]);
+              else
+                mma_bf16_k16(acc[mi][nt], a[mi], bq[0][nt][ks][0], bq[0][nt][ks][1]);
+            }
       }
-    } else {  // NVFP4: dequantize rows g and g+8 of this m-tile to f16 in registers
-      const int r0 = 16 * m + g, r1 = r0 + 8;
-      const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r0 * 64 + 16 * j);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r1 * 64 + 16 * j);
-      const uint16_t sc0 = *reinterpret_cast<const uint16_t*>(scales + r0 * 8 + 2 * j);
-      const uint16_t sc1 = *reinterpret_cast<const uint16_t*>(scales + r1 * 8 + 2 * j);
-      uint32_t s0[2], s1[2];
-      {
+    } else {  // NVFP4: dequantize rows g and g+8 of each m-tile to f16 in registers
+      uint32_t wa[MG][4], wb[MG][4], s0[MG][2], s1[MG][2];
+#pragma unroll
+      for (int mi = 0; mi < MG; ++mi) {
+        const int r0 = 16 * (m0 + mi) + g, r1 = r0 + 8;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(tile + r0 * 64 + 16 * j);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(tile + r1 * 64 + 16 * j);
+        wa[mi][0] = w0.x; wa[mi][1] = w0.y; wa[mi][2] = w0.z; wa[mi][3] = w0.w;
+        wb[mi][0] = w1.x; wb[mi][1] = w1.y; wb[mi][2] = w1.z; wb[mi][3] = w1.w;
+        const uint16_t sc0 = *reinterpret_cast<const uint16_t*>(scales + r0 * 8 + 2 * j);
+        const uint16_t sc1 = *reinterpret_cast<const uint16_t*>(scales + r1 * 8 + 2 * j);
         uint32_t h;
         asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc0));
-        s0[0] = (h & 0xffffu) | (h << 16);
-        s0[1] = (h >> 16) | (h & 0xffff0000u);
+        s0[mi][0] = (h & 0xffffu) | (h << 16);
+        s0[mi][1] = (h >> 16) | (h & 0xffff0000u);
         asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc1));
-        s1[0] = (h & 0xffffu) | (h << 16);
-        s1[1] = (h >> 16) | (h & 0xffff0000u);
+        s1[mi][0] = (h & 0xffffu) | (h << 16);
+        s1[mi][1] = (h >> 16) | (h & 0xffff0000u);
       }
-      const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-      const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        // byte 2ks and 2ks+1 of the lane's 16 bytes hold dims 32j+4ks .. +3
+        // bytes 2ks, 2ks+1 of the lane's 16 bytes hold dims 32j+4ks .. +3
         const int bi = 2 * ks;
-        const uint32_t grp = bi >> 3;  // 0: dims 32j..+15, 1: 32j+16..+31
-        uint32_t a[4];
-        uint32_t x0 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
-        uint32_t x2 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
-        uint32_t x1 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
-        uint32_t x3 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
-        __half2 t;
-        t = __hmul2(*reinterpret_cast<__half2*>(&x0), *reinterpret_cast<const __half2*>(&s0[grp]));
-        a[0] = *reinterpret_cast<uint32_t*>(&t);
-        t = __hmul2(*reinterpret_cast<__half2*>(&x1), *reinterpret_cast<const __half2*>(&s1[grp]));
-        a[1] = *reinterpret_cast<uint32_t*>(&t);
-        t = __hmul2(*reinterpret_cast<__half2*>(&x2), *reinterpret_cast<const __half2*>(&s0[grp]));
-        a[2] = *reinterpret_cast<uint32_t*>(&t);
-        t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[grp]));
-        a[3] = *reinterpret_cast<uint32_t*>(&t);
+        const int grp = bi >> 3;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_k16(acc[nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+        for (int mi = 0; mi < MG; ++mi) {
+          uint32_t x0 = e2m1x2_to_f16x2((wa[mi][bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+          uint32_t x2 = e2m1x2_to_f16x2((wa[mi][bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+          uint32_t x1 = e2m1x2_to_f16x2((wb[mi][bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+          uint32_t x3 = e2m1x2_to_f16x2((wb[mi][bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+          uint32_t a[4];
+          __half2 t;
+          t = __hmul2(*reinterpret_cast<__half2*>(&x0), *reinterpret_cast<const __half2*>(&s0[mi][grp]));
+          a[0] = *reinterpret_cast<uint32_t*>(&t);
+          t = __hmul2(*reinterpret_cast<__half2*>(&x1), *reinterpret_cast<const __half2*>(&s1[mi][grp]));
+          a[1] = *reinterpret_cast<uint32_t*>(&t);
+          t = __hmul2(*reinterpret_cast<__half2*>(&x2), *reinterpret_cast<const __half2*>(&s0[mi][grp]));
+          a[2] = *reinterpret_cast<uint32_t*>(&t);
+          t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[mi][grp]));
+          a[3] = *reinterpret_cast<uint32_t*>(&t);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16_k16(acc[mi][nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+        }
       }
     }
-    // epilogue: rows r0 = 16m + g, r1 = r0 + 8 of this block
-    const int r0 = 16 * m + g, r1 = r0 + 8;
-    float s0 = 1.f, s1 = 1.f;
-    if constexpr (FMT == FMT_FP8) {
-      s0 = reinterpret_cast<const float*>(scales)[r0];
-      s1 = reinterpret_cast<const float*>(scales)[r1];
-    }
-    const int t0 = key0 + r0, t1 = key0 + r1;
+    // epilogue: rows r0 = 16m + g and r0 + 8 of each m-tile
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float v0 = (t0 <= lim_col[nt][c]) ? acc[nt][c] * s0 : -INFINITY;
-        const float v1 = (t1 <= lim_col[nt][c]) ? acc[nt][2 + c] * s1 : -INFINITY;
-        cmax[nt][c] = fmaxf(cmax[nt][c], fmaxf(v0, v1));
+    for (int mi = 0; mi < MG; ++mi) {
+      const int r0 = 16 * (m0 + mi) + g, r1 = r0 + 8;
+      float s0 = 1.f, s1 = 1.f;
+      if constexpr (FMT == FMT_FP8) {
+        s0 = reinterpret_cast<const float*>(scales)[r0];
+        s1 = reinterpret_cast<const float*>(scales)[r1];
       }
+      const int t0 = key0 + r0, t1 = key0 + r1;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float v0 = (t0 <= lim[nt][c]) ? acc[mi][nt][c] * s0 : -INFINITY;
+          const float v1 = (t1 <= lim[nt][c]) ? acc[mi][nt][2 + c] * s1 : -INFINITY;
+          cmax[nt][c] = fmaxf(cmax[nt][c], fmaxf(v0, v1));
+        }
+    }
   }
+}
+
+// Per-unit facts, packed as (code, seq_len): code >= 0 physical block,
+// -1 past the sequence's end, -2 bad data (flag raised), -3 past the last unit.
+__device__ __forceinline__ int2 unit_info(const IndexerParams& p, long u, long total) {
+  const BatchDev& bt = p.batch;
+  if (u >= total) return make_int2(-3, 0);
+  const int s = (int)(u % bt.S), b = (int)(u / bt.S);
+  const int T = bt.seq_len(s);
+  if (T < bt.Q || T > bt.max_nb * kBlock) {
+    if (b == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
+    return make_int2(-2, T);
+  }
+  if (b >= (T + kBlock - 1) / kBlock) return make_int2(-1, T);
+  const int phys = __ldg(bt.row(s) + b);
+  if (phys < 0 || phys >= p.num_blocks) {
+    raise_flag(p.status, FLAG_BAD_BLOCK, phys);
+    return make_int2(-2, T);
+  }
+  return make_int2(phys, T);
 }
 
 template <int FMT, int NT, int SP>
 __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap, const IndexerParams p) {
   using TR = IdxTraits<FMT>;
+  using LY = IdxLayout<FMT>;
   constexpr int KS = TR::KS, NST = TR::NST, WARPS = TR::WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  using LY = IdxLayout<FMT>;
   uint8_t* tiles = base + (size_t)warp * NST * TR::TILE;
   uint8_t* scal = base + LY::SCAL + (size_t)warp * NST * LY::SC;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + LY::BARS) + warp * NST;
-  int* state = reinterpret_cast<int*>(base + LY::STATE) + warp * NST;
 
   const BatchDev bt = p.batch;
   const int S = bt.S, Q = bt.Q, G = p.G;
@@ -191,49 +238,41 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
     fence_mbar_init();
     if constexpr (FMT != FMT_NVFP4) prefetch_tmap(&tmap);
   }
+  // unit facts for iterations [it0, it0 + 64): lane l holds it0 + l and it0 + 32 + l
+  long it0 = 0;
+  int2 inf0 = unit_info(p, gw + (long)lane * tw, total);
+  int2 inf1 = unit_info(p, gw + (long)(32 + lane) * tw, total);
   __syncwarp();
 
-  // lane 0: decide and issue the copy of unit u into stage st
-  auto issue = [&](long u, int st) {
-    const int s = (int)(u % S), b = (int)(u / S);
-    const int T = __ldg(bt.seq_lens + s);
-    int stt = ST_SKIP;
-    if (T < Q || T > bt.max_nb * kBlock) {
-      if (b == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
-      stt = ST_BAD;
-    } else if (b < (T + kBlock - 1) / kBlock) {
-      const int phys = __ldg(bt.block_table + (size_t)s * bt.max_nb + b);
-      if (phys < 0 || phys >= p.num_blocks) {
-        raise_flag(p.status, FLAG_BAD_BLOCK, phys);
-        stt = ST_BAD;
+  auto info_at = [&](long it) -> int2 {
+    const int idx = (int)(it - it0);
+    const int2 v = (idx < 32) ? inf0 : inf1;
+    return make_int2(__shfl_sync(0xffffffffu, v.x, idx & 31), __shfl_sync(0xffffffffu, v.y, idx & 31));
+  };
+  // copy the block of iteration `it` (facts `inf`) into stage st; lane 0 issues
+  auto issue = [&](long it, int2 inf, int st) {
+    if (lane == 0 && inf.x >= 0) {
+      const int phys = inf.x;
+      uint8_t* dst = tiles + (size_t)st * TR::TILE;
+      fence_proxy_async();
+      if constexpr (FMT == FMT_FP8) {
+        mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
+        tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
+        bulk_g2s(scal + (size_t)st * LY::SC, p.idx_scale + (size_t)phys * kBlock, TR::SCALES, &bars[st]);
+      } else if constexpr (FMT == FMT_BF16) {
+        mbar_expect_tx(&bars[st], TR::TILE);
+        tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
+        tma_load_2d(dst + 128 * 128, &tmap, 64, phys * kBlock, &bars[st]);
       } else {
-        stt = ST_LOADED;
-        uint8_t* dst = tiles + (size_t)st * TR::TILE;
-        fence_proxy_async();
-        if constexpr (FMT == FMT_FP8) {
-          mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
-          tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
-          bulk_g2s(scal + (size_t)st * LY::SC, p.idx_scale + (size_t)phys * kBlock, TR::SCALES, &bars[st]);
-        } else if constexpr (FMT == FMT_BF16) {
-          mbar_expect_tx(&bars[st], TR::TILE);
-          tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
-          tma_load_2d(dst + 128 * 128, &tmap, 64, phys * kBlock, &bars[st]);
-        } else {
-          mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
-          bulk_g2s(dst, p.idx + (size_t)phys * TR::TILE, TR::TILE, &bars[st]);
-          bulk_g2s(scal + (size_t)st * LY::SC, p.idx_sf + (size_t)phys * TR::SCALES, TR::SCALES, &bars[st]);
-        }
+        mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
+        bulk_g2s(dst, p.idx + (size_t)phys * TR::TILE, TR::TILE, &bars[st]);
+        bulk_g2s(scal + (size_t)st * LY::SC, p.idx_sf + (size_t)phys * TR::SCALES, TR::SCALES, &bars[st]);
       }
     }
-    state[st] = stt;
   };
 
-  if (lane == 0)
-    for (int st = 0; st < NST; ++st)
-      if (gw + (long)st * tw < total) issue(gw + (long)st * tw, st);
-  __syncwarp();
-  // the query fragments come from the preceding kernel (programmatic launch)
-  pdl_wait();
+#pragma unroll
+  for (int st = 0; st < NST; ++st) issue(st, info_at(st), st);
 
   uint32_t phase_bits = 0;
   int cur_s = -1;
@@ -241,31 +280,32 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
   float colf[NT][2];
   bool dead = false;
 
-  int it = 0;
-  for (long u = gw; u < total; u += tw, ++it) {
-    const int st = it % NST;
+  for (long it = 0;; ++it) {
+    if (it - it0 == 32) {  // slide the window of unit facts
+      inf0 = inf1;
+      it0 += 32;
+      inf1 = unit_info(p, gw + (it0 + 32 + lane) * tw, total);
+    }
+    const int2 inf = info_at(it);
+    if (inf.x == -3) break;
+    const long u = gw + it * tw;
+    const int st = (int)(it % NST);
     const int s = (int)(u % S), b = (int)(u / S);
-    const int stt = state[st];
     float* prow = p.pooled + (size_t)s * Q * G * bt.max_nb + b;
-    if (stt == ST_LOADED && !dead) {
+    if (inf.x >= 0 && !dead) {
       if (s != cur_s) {
         cur_s = s;
-        const uint32_t* fr = p.qfrag + (size_t)s * p.geom.words_per_unit();
+        // the query fragments come from the caller's index_q; a preceding kernel may still be writing it
+        pdl_wait();
+        long rows[NT];
 #pragma unroll
-        for (int sp = 0; sp < SP; ++sp)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-              for (int rg = 0; rg < 2; ++rg)
-                bq[sp][nt][ks][rg] = __ldg(fr + ((((sp * NT + nt) * KS + ks) * 2 + rg) * 32) + lane);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) colf[nt][c] = __ldg(p.colf + (size_t)s * NT * 8 + nt * 8 + 2 * (lane & 3) + c);
+        for (int nt = 0; nt < NT; ++nt) {
+          const int col = nt * 8 + (lane >> 2);
+          rows[nt] = (col < Q * G) ? ((long)s * Q * G + col) * kDim : -1;
+        }
+        build_qfrag<FMT, NT, SP, KS>(p.index_q, p.iq_fp8, rows, p.iq_scale, p.col_const, bq, colf, lane);
       }
-      const int T = __ldg(bt.seq_lens + s);
+      const int T = inf.y;
       int lim[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -283,8 +323,8 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
         float cmax[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) cmax[nt][0] = cmax[nt][1] = -INFINITY;
-        score_block<FMT, NT, SP>(tiles + (size_t)st * TR::TILE, scal + (size_t)st * LY::SC, bq,
-                                 lane, b * kBlock, lim, cmax);
+        score_block<FMT, NT, SP>(tiles + (size_t)st * TR::TILE, scal + (size_t)st * LY::SC, bq, lane, b * kBlock,
+                                 lim, cmax);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -297,12 +337,12 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
             if (lane < 4 && col < Q * G) prow[(size_t)col * bt.max_nb] = v * colf[nt][c];
           }
       }
-    } else if (stt != ST_LOADED || dead) {
+    }
+    if (inf.x < 0 || dead) {
       for (int col = lane; col < Q * G; col += 32) prow[(size_t)col * bt.max_nb] = -INFINITY;
     }
     __syncwarp();
-    if (!dead && lane == 0 && u + (long)NST * tw < total) issue(u + (long)NST * tw, st);
-    __syncwarp();
+    if (!dead) issue(it + NST, info_at(it + NST), st);
   }
   pdl_launch_dependents();
   // a warp that gave up waits (bounded) for copies still in flight before exiting

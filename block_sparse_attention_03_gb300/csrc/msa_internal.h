@@ -15,13 +15,31 @@ struct DeviceStatus;
 // Element formats as the kernels see them.
 enum Fmt : int { FMT_BF16 = 0, FMT_FP8 = 1, FMT_NVFP4 = 2 };
 
+// The batch as the kernels see it.  A long chunk of new tokens (prefill) is
+// split into `chunks` virtual sequences of Q tokens each: virtual sequence s
+// is chunk s % chunks of real sequence s / chunks, sharing its block table,
+// with its length ending at the chunk's last token.  Query rows keep the real
+// token-major order (virtual row s*Q + i == real row).
 struct BatchDev {
   const int32_t* seq_lens;
   const int32_t* block_table;
-  int32_t S, Q, max_nb;
+  int32_t S, Q, max_nb;  // virtual sequences and their query tokens
+  int32_t chunks;        // virtual sequences per real sequence (1: none)
+  int32_t q_real;        // new tokens per real sequence (= Q * chunks)
+
+  // length of (virtual) sequence s; -1 if its real sequence is malformed
+  __device__ __forceinline__ int seq_len(int s) const {
+    if (chunks == 1) return __ldg(seq_lens + s);
+    const int T = __ldg(seq_lens + s / chunks);
+    if (T < q_real) return -1;
+    return T - q_real + Q * (s % chunks + 1);
+  }
+  __device__ __forceinline__ const int32_t* row(int s) const {
+    return block_table + (size_t)(chunks == 1 ? s : s / chunks) * max_nb;
+  }
 };
 
-// Query-fragment geometry of one MMA operand set (see msa_prep.cu).
+// Query-fragment geometry of one MMA operand set (see msa_qfrag.cuh).
 //   cols: query columns (rows of the query matrix) per unit
 //   sp:   number of split terms (2: bf16 -> e4m3 hi + lo; else 1)
 //   nt:   8-column tiles = ceil(cols / 8)
@@ -31,18 +49,6 @@ struct FragGeom {
   __host__ __device__ int32_t words_per_unit() const { return sp * nt * ks * 2 * 32; }
 };
 
-struct PrepParams {
-  const void* q;       // [units][cols][128] queries (bf16 or e4m3 codes)
-  int32_t q_is_fp8;
-  float q_scale;       // per-tensor scale of e4m3 queries
-  float col_const;     // extra constant folded into every column factor
-  int32_t key_fmt;     // operand format of the other side (Fmt)
-  FragGeom geom;
-  int32_t units;
-  uint32_t* frag;      // [units][words_per_unit]
-  float* colf;         // [units][nt * 8]
-};
-
 struct IndexerParams {
   BatchDev batch;
   int32_t G;
@@ -50,8 +56,10 @@ struct IndexerParams {
   const uint8_t* idx;      // raw cache (NVFP4 path)
   const uint8_t* idx_sf;   // NVFP4 scales
   const float* idx_scale;  // FP8 per-token scales
-  const uint32_t* qfrag;   // [S][words]
-  const float* colf;       // [S][nt*8]
+  const void* index_q;     // [S*Q][G][128] bf16 or e4m3 codes
+  int32_t iq_fp8;
+  float iq_scale;          // per-tensor scale of e4m3 index queries
+  float col_const;         // index_scale (x NVFP4 per-tensor scale)
   FragGeom geom;
   float* pooled;           // [S*Q][G][max_nb]
   DeviceStatus* status;
@@ -63,6 +71,16 @@ struct TopkParams {
   const float* pooled;
   int32_t* topk_idx;
   float* topk_score;
+  int32_t* zero;            // attend work counters to clear (nullable)
+  int32_t nzero;
+  // attend query fragments for unit (s, g), written when frag != null
+  const void* q;
+  int32_t q_fp8;
+  float q_scale, col_const;
+  int32_t key_fmt, r, hq;
+  FragGeom geom;
+  uint32_t* frag;           // [S*G][geom.words_per_unit()]
+  float* colf;              // [S*G][geom.nt*8]
   DeviceStatus* status;
 };
 
@@ -74,6 +92,16 @@ struct UnionParams {
   int32_t* u_ids;           // [S][G][cap]
   uint32_t* u_mask;         // [S][G][cap]
   int32_t* u_count;         // [S][G]
+  int32_t* zero;            // attend work counters to clear (nullable)
+  int32_t nzero;
+  // attend query fragments for unit (s, g), written when frag != null
+  const void* q;
+  int32_t q_fp8;
+  float q_scale, col_const;
+  int32_t key_fmt, r, hq;
+  FragGeom geom;
+  uint32_t* frag;           // [S*G][geom.words_per_unit()]
+  float* colf;              // [S*G][geom.nt*8]
   DeviceStatus* status;
 };
 
@@ -87,39 +115,39 @@ struct AttendParams {
   const uint8_t* v_sf;
   const float* k_scale;
   const float* v_scale;
-  float v_global;           // NVFP4 V per-tensor scale (K's is folded into colf)
-  const uint32_t* qfrag;    // [S*G][words]
-  const float* colf;        // [S*G][nt*8]  (log2-domain logit factor per column)
+  float v_global;           // NVFP4 V per-tensor scale (K's is folded into col_const)
+  const void* q;            // [S*Q][G*r][128] bf16 or e4m3 codes
+  int32_t q_fp8;
+  float q_scale;
+  float col_const;          // sm_scale * log2(e) (x NVFP4 K per-tensor scale)
   FragGeom geom;
-  const int32_t* u_ids;
+  int32_t direct;           // 1: single query token, read the selection rows directly
+  const int32_t* topk_idx;  // direct mode: [S][G][topk]
+  int32_t topk;
+  const int32_t* u_ids;     // union mode
   const uint32_t* u_mask;
   const int32_t* u_count;
   int32_t cap;
-  int32_t bps;              // union blocks per split
+  int32_t bps;              // selected blocks per split
   int32_t splits;
+  const uint32_t* frag;     // [S*G][geom.words_per_unit()] query fragments (preceding kernel)
+  const float* colf;        // [S*G][geom.nt*8] column factors
+  int32_t* work_ctr;        // unit counter (zeroed by the preceding kernel)
+  int32_t* sg_ctr;          // [S*G] partials written per (sequence, group) (zeroed likewise)
   float* part_o;            // [S*G][splits][cols][128]
   float* part_ml;           // [S*G][splits][cols][2]
+  void* out;                // bf16 [S*Q][G*r][128]
+  float* lse;               // [S*Q][G*r] or null
   DeviceStatus* status;
 };
 
-struct CombineParams {
-  int32_t S, Q, G, r, splits, cols;
-  const float* part_o;
-  const float* part_ml;
-  void* out;   // bf16 [S*Q][G*r][128]
-  float* lse;  // [S*Q][G*r] or null
-};
-
 // launchers (return cudaGetLastError())
-cudaError_t launch_prep_rows(const PrepParams& p, int a, int u2, int b, int c2, int c, cudaStream_t st);
-int attend_max_stages(int fmt);
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
                            bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attend(int fmt, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, const AttendParams& p,
-                          cudaStream_t st, bool pdl);
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
+                          int num_sms, cudaStream_t st, bool pdl);
 cudaError_t launch_dequant(int fmt, int which, const msa_cache_t& c, const int32_t* phys, int32_t n, float* out,
                            cudaStream_t st);
 

@@ -17,12 +17,26 @@
 // contiguous id range.
 #include "msa_device.cuh"
 #include "msa_internal.h"
+#include "msa_qfrag.cuh"
 
 namespace msa {
 
 namespace {
 
 constexpr int kTopkThreads = 256;
+constexpr int kKeysPerThread = 16;
+
+// Histogram increment aggregated over the lanes of a warp that hit the same
+// bin (the order keys of close scores share their top bits, so plain atomics
+// would serialise on one bin).  Every lane of the warp must call it.
+__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const uint32_t peers = __match_any_sync(act, bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+constexpr int kMaxFragCols = 32;
 
 // block-wide exclusive scan of one int per thread; returns the total
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& excl) {
@@ -52,10 +66,24 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
 
   pdl_wait();
   const BatchDev bt = p.batch;
+  if (p.zero) {  // clear the attend's work counters for this call
+    const int z = blockIdx.x * blockDim.x + threadIdx.x;
+    if (z < p.nzero) p.zero[z] = 0;
+  }
   const int row = blockIdx.x;  // (s*Q + i) * G + g
+  if (row >= bt.S * bt.Q * p.G) return;  // extra CTAs only clear counters
+  if (p.frag) {
+    // one query token: this CTA's row is attend unit (s, g); build its query fragments
+    __shared__ float qs[kMaxFragCols * (kDim + 1)];
+    __shared__ float pscale[kMaxFragCols];
+    const int s_ = row / p.G, g_ = row % p.G, r = p.r, hq = p.hq, cols = p.geom.cols;
+    auto row_of = [&](int col) -> long { return col < cols ? ((long)s_ * hq + g_ * r + col) * kDim : -1l; };
+    write_qfrag(p.q, p.q_fp8, row_of, p.q_scale, p.col_const, p.key_fmt, p.geom, qs, pscale,
+                p.frag + (size_t)row * p.geom.words_per_unit(), p.colf + (size_t)row * p.geom.nt * 8);
+  }
   const int sq = row / p.G;
   const int s = sq / bt.Q, i = sq % bt.Q;
-  const int T = bt.seq_lens[s];
+  const int T = bt.seq_len(s);
   const int K = p.topk;
   int32_t* out = p.topk_idx + (size_t)row * K;
   float* out_sc = p.topk_score ? p.topk_score + (size_t)row * K : nullptr;
@@ -83,6 +111,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const int b0 = lo + threadIdx.x * per;
   const int b1 = min(hi, b0 + per);
 
+  // this thread's candidate keys stay in registers across the passes (rows of
+  // up to kTopkThreads * kKeysPerThread candidates; longer rows re-read them)
+  const int cnt = max(0, b1 - b0);
+  const bool inreg = per <= kKeysPerThread;
+  uint32_t keys[kKeysPerThread];
+#pragma unroll
+  for (int i = 0; i < kKeysPerThread; ++i) keys[i] = (inreg && i < cnt) ? float_order_key(pr[b0 + i]) : 0u;
+  auto key_at = [&](int i) -> uint32_t { return float_order_key(pr[b0 + i]); };
+
   uint32_t thr = 0;     // keys > thr are taken; keys == thr: the first `need_eq` by id
   int need_eq = 0;
   const bool take_all = ncand <= kfree;
@@ -94,9 +131,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
       const int shift = 24 - 8 * pass;
       for (int k = threadIdx.x; k < 256; k += blockDim.x) hist[k] = 0;
       __syncthreads();
-      for (int b = b0; b < b1; ++b) {
-        const uint32_t key = float_order_key(pr[b]);
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+      if (inreg) {
+#pragma unroll
+        for (int i = 0; i < kKeysPerThread; ++i)
+          hist_add(hist, (keys[i] >> shift) & 255, i < cnt && (keys[i] & pmask) == prefix);
+      } else {
+        for (int i = 0; i < cnt; ++i) {
+          const uint32_t key = key_at(i);
+          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+        }
       }
       __syncthreads();
       if (threadIdx.x < 32) {
@@ -136,34 +179,48 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   // count this thread's takes, in id order
   int n_gt = 0, n_eq = 0;
   if (!take_all && !take_none) {
-    for (int b = b0; b < b1; ++b) {
-      const uint32_t key = float_order_key(pr[b]);
-      n_gt += key > thr;
-      n_eq += key == thr;
+    if (inreg) {
+#pragma unroll
+      for (int i = 0; i < kKeysPerThread; ++i)
+        if (i < cnt) {
+          n_gt += keys[i] > thr;
+          n_eq += keys[i] == thr;
+        }
+    } else {
+      for (int i = 0; i < cnt; ++i) {
+        const uint32_t key = key_at(i);
+        n_gt += key > thr;
+        n_eq += key == thr;
+      }
     }
   }
   int eq_before = 0;
   block_exclusive_scan(n_eq, warp_tot, eq_before);
   const int eq_take = (take_all || take_none) ? 0 : max(0, min(n_eq, need_eq - eq_before));
-  const int my_take = take_all ? (b1 > b0 ? b1 - b0 : 0) : (take_none ? 0 : n_gt + eq_take);
+  const int my_take = take_all ? cnt : (take_none ? 0 : n_gt + eq_take);
   int base = 0;
   const int n_sel = block_exclusive_scan(my_take, warp_tot, base);
 
   // ascending output: [0, n_init) ++ selected ++ [hi, recent]
   int o = n_init + base;
   int eq_seen = 0;
-  for (int b = b0; b < b1 && !take_none; ++b) {
-    const float v = pr[b];
-    bool take = take_all;
-    if (!take_all) {
-      const uint32_t key = float_order_key(v);
-      if (key > thr) take = true;
-      else if (key == thr) take = (eq_seen++ < eq_take);
-    }
-    if (take) {
-      out[o] = b;
-      if (out_sc) out_sc[o] = v;
-      ++o;
+  if (!take_none) {
+    for (int i = 0; i < cnt; ++i) {
+      const uint32_t key = inreg ? keys[0] : key_at(i);
+      bool take = take_all;
+      if (!take_all) {
+        if (key > thr) take = true;
+        else if (key == thr) take = (eq_seen++ < eq_take);
+      }
+      if (take) {
+        out[o] = b0 + i;
+        if (out_sc) out_sc[o] = pr[b0 + i];
+        ++o;
+      }
+      if (inreg) {  // shift the register window (keeps the keys array in registers)
+#pragma unroll
+        for (int t = 0; t + 1 < kKeysPerThread; ++t) keys[t] = keys[t + 1];
+      }
     }
   }
   const int tail0 = n_init + n_sel;
@@ -189,10 +246,24 @@ __global__ void __launch_bounds__(256) union_kernel(const UnionParams p) {
   int* first = sh + p.cap;                            // [cap] 1 if first occurrence
   uint32_t* masks = reinterpret_cast<uint32_t*>(sh + 2 * p.cap);  // [cap]
   pdl_wait();
+  if (p.zero) {  // clear the attend's work counters for this call
+    for (int z = blockIdx.x * blockDim.x + threadIdx.x; z < p.nzero; z += gridDim.x * blockDim.x) p.zero[z] = 0;
+  }
   const BatchDev bt = p.batch;
   const int unit = blockIdx.x;  // s * G + g
   const int s = unit / p.G, g = unit % p.G;
-  const int T = bt.seq_lens[s];
+  if (p.frag) {
+    __shared__ float qs[kMaxFragCols * (kDim + 1)];
+    __shared__ float pscale[kMaxFragCols];
+    const int r = p.r, hq = p.hq, cols = p.geom.cols, Q = bt.Q;
+    auto row_of = [&](int col) -> long {
+      return col < cols ? ((long)(s * Q + col / r) * hq + g * r + col % r) * kDim : -1l;
+    };
+    write_qfrag(p.q, p.q_fp8, row_of, p.q_scale, p.col_const, p.key_fmt, p.geom, qs, pscale,
+                p.frag + (size_t)unit * p.geom.words_per_unit(), p.colf + (size_t)unit * p.geom.nt * 8);
+    __syncthreads();
+  }
+  const int T = bt.seq_len(s);
   const int n = bt.Q * p.topk;
   const bool seq_ok = !(T < bt.Q || T > bt.max_nb * kBlock);
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
@@ -253,7 +324,8 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   const unsigned rows = (unsigned)(p.batch.S * p.batch.Q * p.G);
-  cudaLaunchConfig_t cfg = make_cfg(dim3(rows), dim3(kTopkThreads), 0, st, pdl, attr);
+  const unsigned zrows = (unsigned)((p.nzero + kTopkThreads - 1) / kTopkThreads);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(kTopkThreads), 0, st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, topk_kernel, p);
 }
 

@@ -63,7 +63,7 @@ def test_workspace_size_host_only(lib):
     assert n > 0
     assert lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 15) == 0
     for over in ({"f__topk": 12}, {"c__block_size": 64}, {"c__head_dim": 64}, {"b__num_seqs": 0},
-                 {"f__init_blocks": 16}, {"b__q_per_seq": 33}, {"c__num_kv_heads": 9}):
+                 {"f__init_blocks": 16}, {"b__q_per_seq": 50 * 128 + 1}, {"c__num_kv_heads": 9}):
         c2, b2, f2 = _structs(**over)
         assert lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) == 0, over
     # more sequences or blocks never shrink the workspace

@@ -57,6 +57,12 @@ STAGED_CASES = [
     ("fp8_decode", dict(seq_lens=(3000, 2000), q_per_seq=4, seed=16)),  # bf16 q, multi-token FP8
     ("tiny_bf16", dict(seq_lens=(2000, 1500), kv_dtype="fp8", index_dtype="nvfp4", seed=17)),
     ("tiny_bf16", dict(seq_lens=(2000,), kv_dtype="nvfp4", index_dtype="bf16", q_dtype="fp8", seed=18)),
+    # prefill chunks: more than 8 new tokens are split into 8/4/2/1-token virtual sequences
+    ("fp8_prefill", dict(seq_lens=(2000 + 64,), q_per_seq=64, seed=19)),
+    ("fp8_prefill", dict(seq_lens=(1500, 900), q_per_seq=24, seed=20)),
+    ("fp8_decode", dict(seq_lens=(700, 900), q_per_seq=12, seed=22)),
+    ("tiny_bf16", dict(seq_lens=(1000,), q_per_seq=33, kv_dtype="nvfp4", index_dtype="nvfp4", q_dtype="fp8",
+                       seed=23)),
 ]
 
 
@@ -186,3 +192,20 @@ def test_full_size_sampled(name, seqs):
         check_selection(g["topk"], full, w.seq_lens, Q, w.topk, rows=rows)
         o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
         check_out(g["out"][rows], o)
+
+
+def test_full_size_prefill_sampled():
+    # 8,192 new tokens on a 64K-token FP8 context: sampled query rows against the oracle
+    w = ms.make_workload("fp8_prefill")
+    c = ms.make_case(w, device="cuda")
+    g = gpu_path(c)
+    h = ms.case_to_host(c)
+    del c
+    torch.cuda.empty_cache()
+    rows = [0, 1, 7, 8, 2047, 4096, 8190, 8191]
+    pooled = O.pooled_scores(h, 0, w.index_dim ** -0.5, rows=rows)
+    full = np.full((w.q_per_seq, w.num_kv_heads, w.max_blocks), -np.inf)
+    full[rows] = pooled
+    check_selection(g["topk"], full, w.seq_lens, w.q_per_seq, w.topk, rows=rows)
+    o, _ = O.attend_rows(h, 0, g["topk"], w.head_dim ** -0.5, rows=rows)
+    check_out(g["out"][rows], o)
