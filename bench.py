@@ -292,8 +292,29 @@ def main():
         msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws, stream)
         ievs[i][1].record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     idx_ms = sum(a.elapsed_time(b) for a, b in ievs) / args.steps
+
+    # the other stages alone (through their own entry points), for the breakdown
+    def time_stage(fn, n=10):
+        evs_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        fn()
+        for i in range(n):
+            flush()
+            evs_[i][0].record(stream)
+            fn()
+            evs_[i][1].record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * sum(a.elapsed_time(b) for a, b in evs_) / n
+
+    topk2 = torch.empty_like(topk)
+    out2 = torch.empty_like(out)
+    stages_us = {
+        "indexer": 1e3 * idx_ms,
+        "topk": time_stage(lambda: msa.msa_topk_blocks(batch, cfg, w.num_kv_heads, pooled, topk2, None, ws, stream)),
+        "union+attend": time_stage(lambda: msa.msa_sparse_attend(cache, batch, cfg, q, w.num_q_heads, topk2, out2,
+                                                                 None, ws, stream)),
+    }
+    clocks = sampler.stop()
 
     # ---------------- end to end through the public API with host buffers
     h_iq = torch.empty_like(case["index_q"], device="cpu").pin_memory()
@@ -370,6 +391,7 @@ def main():
             "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "flushed before every timed step (256 MB write, then 512 MB read)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "path_hbm_gbs": path_gbs, "path_frac_of_peak": path_gbs / peak,
+            "stages_us_alone": stages_us,
             "bytes_per_step": {"algorithmic": step_bytes, "index": idx_bytes, "kv_selected": kv_bytes,
                                "with_fp32_scales": actual_bytes},
             "roofline": ({"bound": "hbm", "kernel": "indexer_kernel (score + block max-pool)", "achieved": idx_gbs,

@@ -54,14 +54,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Wait until the phase with the given parity completes.  Bounded: returns
-// false after ~max_tries polls (each poll may suspend up to ~20 us).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 200000) {
+// Wait until the phase with the given parity completes.  Bounded: each
+// try_wait returns after a short, implementation-defined time if the phase is
+// still open; after ~max_tries of them (a few seconds at most) it gives up and
+// returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 4000000) {
   const uint32_t a = smem_u32(bar);
   for (int i = 0; i < max_tries; ++i) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
         : "r"(a), "r"(parity)
         : "memory");
@@ -71,12 +73,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int ma
 }
 
 // Warp-uniform wait: every lane polls, the warp agrees on the outcome.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int max_tries = 200000) {
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int max_tries = 4000000) {
   const uint32_t a = smem_u32(bar);
   for (int i = 0; i < max_tries; ++i) {
     uint32_t done;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
         : "=r"(done)
         : "r"(a), "r"(parity)
         : "memory");

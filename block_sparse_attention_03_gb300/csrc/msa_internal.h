@@ -141,6 +141,16 @@ struct AttendParams {
   DeviceStatus* status;
 };
 
+struct CombineParams {
+  int32_t S, Q, G, r, splits, cols, bps, topk, direct;
+  const int32_t* topk_idx;  // direct mode: [S][G][topk]
+  const int32_t* u_count;   // union mode: [S][G]
+  const float* part_o;
+  const float* part_ml;
+  void* out;   // bf16 [S*Q][G*r][128]
+  float* lse;  // [S*Q][G*r] or null
+};
+
 // launchers (return cudaGetLastError())
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
                            bool pdl);
@@ -148,6 +158,8 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attend(int fmt, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, const AttendParams& p,
                           int num_sms, cudaStream_t st, bool pdl);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
+int attend_stages(int fmt, int nt);  // blocks one attend CTA holds in flight (= blocks per split)
 cudaError_t launch_dequant(int fmt, int which, const msa_cache_t& c, const int32_t* phys, int32_t n, float* out,
                            cudaStream_t st);
 

@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kTopkThreads = 256;
 constexpr int kKeysPerThread = 16;
+constexpr int kRankMax = 1024;  // rows up to this many candidates use the rank test
 
 // Histogram increment aggregated over the lanes of a warp that hit the same
 // bin (the order keys of close scores share their top bits, so plain atomics
@@ -39,6 +40,7 @@ __device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
 constexpr int kMaxFragCols = 32;
 
 // block-wide exclusive scan of one int per thread; returns the total
+template <int THREADS>
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& excl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -49,7 +51,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& e
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   int wbase = 0, total = 0;
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
+  for (int w = 0; w < THREADS / 32; ++w) {
     const int t = warp_tot[w];
     if (w < warp) wbase += t;
     total += t;
@@ -59,9 +61,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& e
   return total;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) {
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
   __shared__ int hist[256];
-  __shared__ int warp_tot[kTopkThreads / 32];
+  __shared__ int warp_tot[THREADS / 32];
   __shared__ uint32_t sh_prefix, sh_need;
 
   pdl_wait();
@@ -107,9 +110,56 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
   const int kfree = K - n_init - n_local - 1;
 
   // thread-owned contiguous candidate range
-  const int per = (ncand + kTopkThreads - 1) / kTopkThreads;
+  const int per = (ncand + THREADS - 1) / THREADS;
   const int b0 = lo + threadIdx.x * per;
   const int b1 = min(hi, b0 + per);
+
+  // ---------------- short rows: rank test against every other candidate
+  // A candidate is kept iff fewer than kfree candidates beat it (a higher
+  // score, or the same score and a smaller id).  One pass over the row in
+  // shared memory (broadcast reads), no histogram passes.
+  if (ncand > kfree && kfree > 0 && ncand <= kRankMax) {
+    __shared__ uint32_t rk[kRankMax];
+    for (int c = threadIdx.x; c < ncand; c += THREADS) rk[c] = float_order_key(pr[lo + c]);
+    __syncthreads();
+    // thread t owns candidates [t*per_r, (t+1)*per_r): contiguous ids, so the
+    // selected ones come out in ascending order after one exclusive scan
+    const int per_r = (ncand + THREADS - 1) / THREADS;
+    const int c0 = threadIdx.x * per_r, c1 = min(ncand, c0 + per_r);
+    uint32_t selbits = 0;
+    for (int c = c0; c < c1; ++c) {
+      const uint32_t kc = rk[c];
+      int beat = 0;
+      for (int x = 0; x < ncand; ++x) {
+        const uint32_t kx = rk[x];
+        beat += (kx > kc) || (kx == kc && x < c);
+      }
+      if (beat < kfree) selbits |= 1u << (c - c0);
+    }
+    int base_r = 0;
+    const int n_sel_r = block_exclusive_scan<THREADS>(__popc(selbits), warp_tot, base_r);
+    int o_r = n_init + base_r;
+    for (int c = c0; c < c1; ++c)
+      if (selbits & (1u << (c - c0))) {
+        out[o_r] = lo + c;
+        if (out_sc) out_sc[o_r] = pr[lo + c];
+        ++o_r;
+      }
+    const int tail_r = n_init + n_sel_r;
+    for (int k = threadIdx.x; k < K; k += THREADS) {
+      if (k < n_init) {
+        out[k] = k;
+        if (out_sc) out_sc[k] = pr[k];
+      } else if (k >= tail_r) {
+        const int b = hi + (k - tail_r);
+        const bool real = b <= recent;
+        out[k] = real ? b : -1;
+        if (out_sc) out_sc[k] = real ? pr[b] : -INFINITY;
+      }
+    }
+    pdl_launch_dependents();
+    return;
+  }
 
   // this thread's candidate keys stay in registers across the passes (rows of
   // up to kTopkThreads * kKeysPerThread candidates; longer rows re-read them)
@@ -195,11 +245,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p) 
     }
   }
   int eq_before = 0;
-  block_exclusive_scan(n_eq, warp_tot, eq_before);
+  block_exclusive_scan<THREADS>(n_eq, warp_tot, eq_before);
   const int eq_take = (take_all || take_none) ? 0 : max(0, min(n_eq, need_eq - eq_before));
   const int my_take = take_all ? cnt : (take_none ? 0 : n_gt + eq_take);
   int base = 0;
-  const int n_sel = block_exclusive_scan(my_take, warp_tot, base);
+  const int n_sel = block_exclusive_scan<THREADS>(my_take, warp_tot, base);
 
   // ascending output: [0, n_init) ++ selected ++ [hi, recent]
   int o = n_init + base;
@@ -324,9 +374,13 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   const unsigned rows = (unsigned)(p.batch.S * p.batch.Q * p.G);
-  const unsigned zrows = (unsigned)((p.nzero + kTopkThreads - 1) / kTopkThreads);
-  cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(kTopkThreads), 0, st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+  // long rows: 1024 threads (more warps to hide latency, 4x fewer keys each)
+  const bool wide = p.batch.max_nb > 1024;
+  const unsigned threads = wide ? 1024u : (unsigned)kTopkThreads;
+  const unsigned zrows = (unsigned)((p.nzero + threads - 1) / threads);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(threads), 0, st, pdl, attr);
+  if (wide) return cudaLaunchKernelEx(&cfg, topk_kernel<1024>, p);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<kTopkThreads>, p);
 }
 
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl) {
