@@ -10,11 +10,17 @@
 //
 // Kernel: one CTA per (query row, group).  The free candidates form one
 // contiguous id range [lo, hi) (everything between the forced init and local
-// blocks), so a radix select over order-preserving 32-bit keys (4 passes of
-// 8 bits, shared-memory histograms) finds the k'-th largest score; ties at the
-// threshold are resolved by id through a block-wide prefix count, and the
-// final ids come out ascending without a sort because each thread owns a
-// contiguous id range.
+// blocks), split into one contiguous id range per thread, keys in registers.
+// Main path (threshold + rank test): the candidates are cut into 32 groups of
+// consecutive threads; the kfree-th largest group maximum T is a lower bound
+// with at least kfree candidates >= T, so the wanted kfree (by score, then id)
+// are all among the candidates >= T -- typically a few dozen.  Those are
+// compacted in id order into shared memory and each is kept iff fewer than
+// kfree of them beat it.  Rows where that set is large (heavy ties) take a
+// radix select over order-preserving 32-bit keys (4 passes of 8 bits,
+// shared-memory histograms) with ties at the threshold resolved by id through
+// a block-wide prefix count.  Either way the ids come out ascending without a
+// sort because each thread owns a contiguous id range.
 #include "msa_device.cuh"
 #include "msa_internal.h"
 #include "msa_qfrag.cuh"
@@ -24,8 +30,9 @@ namespace msa {
 namespace {
 
 constexpr int kTopkThreads = 256;
-constexpr int kKeysPerThread = 16;
-constexpr int kRankMax = 1024;  // rows up to this many candidates use the rank test
+constexpr int kKeysPerThreadNarrow = 16;  // keys each thread holds in registers (256 threads)
+constexpr int kKeysPerThreadWide = 8;     // (1024 threads)
+constexpr int kCandMax = 1024;            // candidates >= T the rank test takes; more go to the radix select
 
 // Histogram increment aggregated over the lanes of a warp that hit the same
 // bin (the order keys of close scores share their top bits, so plain atomics
@@ -63,20 +70,22 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& e
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
+  constexpr int kKeysPerThread = THREADS >= 1024 ? kKeysPerThreadWide : kKeysPerThreadNarrow;
+  static_assert(THREADS % 32 == 0 && THREADS >= 32 && THREADS <= 1024, "thread count");
   __shared__ int hist[256];
   __shared__ int warp_tot[THREADS / 32];
   __shared__ uint32_t sh_prefix, sh_need;
+  __shared__ uint32_t gmax[32];
+  __shared__ uint32_t ck[kCandMax];
+  __shared__ uint8_t csel[kCandMax];
 
-  pdl_wait();
   const BatchDev bt = p.batch;
-  if (p.zero) {  // clear the attend's work counters for this call
-    const int z = blockIdx.x * blockDim.x + threadIdx.x;
-    if (z < p.nzero) p.zero[z] = 0;
-  }
   const int row = blockIdx.x;  // (s*Q + i) * G + g
-  if (row >= bt.S * bt.Q * p.G) return;  // extra CTAs only clear counters
-  if (p.frag) {
-    // one query token: this CTA's row is attend unit (s, g); build its query fragments
+  const bool real_row = row < bt.S * bt.Q * p.G;
+  if (real_row && p.frag) {
+    // one query token: this CTA's row is attend unit (s, g); build its query
+    // fragments.  They come from the caller's q alone, so this overlaps the
+    // indexer still running ahead of this kernel.
     __shared__ float qs[kMaxFragCols * (kDim + 1)];
     __shared__ float pscale[kMaxFragCols];
     const int s_ = row / p.G, g_ = row % p.G, r = p.r, hq = p.hq, cols = p.geom.cols;
@@ -84,6 +93,12 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
     write_qfrag(p.q, p.q_fp8, row_of, p.q_scale, p.col_const, p.key_fmt, p.geom, qs, pscale,
                 p.frag + (size_t)row * p.geom.words_per_unit(), p.colf + (size_t)row * p.geom.nt * 8);
   }
+  pdl_wait();
+  if (p.zero) {  // clear the attend's work counters for this call
+    const int z = blockIdx.x * blockDim.x + threadIdx.x;
+    if (z < p.nzero) p.zero[z] = 0;
+  }
+  if (!real_row) return;  // extra CTAs only clear counters
   const int sq = row / p.G;
   const int s = sq / bt.Q, i = sq % bt.Q;
   const int T = bt.seq_len(s);
@@ -114,55 +129,8 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
   const int b0 = lo + threadIdx.x * per;
   const int b1 = min(hi, b0 + per);
 
-  // ---------------- short rows: rank test against every other candidate
-  // A candidate is kept iff fewer than kfree candidates beat it (a higher
-  // score, or the same score and a smaller id).  One pass over the row in
-  // shared memory (broadcast reads), no histogram passes.
-  if (ncand > kfree && kfree > 0 && ncand <= kRankMax) {
-    __shared__ uint32_t rk[kRankMax];
-    for (int c = threadIdx.x; c < ncand; c += THREADS) rk[c] = float_order_key(pr[lo + c]);
-    __syncthreads();
-    // thread t owns candidates [t*per_r, (t+1)*per_r): contiguous ids, so the
-    // selected ones come out in ascending order after one exclusive scan
-    const int per_r = (ncand + THREADS - 1) / THREADS;
-    const int c0 = threadIdx.x * per_r, c1 = min(ncand, c0 + per_r);
-    uint32_t selbits = 0;
-    for (int c = c0; c < c1; ++c) {
-      const uint32_t kc = rk[c];
-      int beat = 0;
-      for (int x = 0; x < ncand; ++x) {
-        const uint32_t kx = rk[x];
-        beat += (kx > kc) || (kx == kc && x < c);
-      }
-      if (beat < kfree) selbits |= 1u << (c - c0);
-    }
-    int base_r = 0;
-    const int n_sel_r = block_exclusive_scan<THREADS>(__popc(selbits), warp_tot, base_r);
-    int o_r = n_init + base_r;
-    for (int c = c0; c < c1; ++c)
-      if (selbits & (1u << (c - c0))) {
-        out[o_r] = lo + c;
-        if (out_sc) out_sc[o_r] = pr[lo + c];
-        ++o_r;
-      }
-    const int tail_r = n_init + n_sel_r;
-    for (int k = threadIdx.x; k < K; k += THREADS) {
-      if (k < n_init) {
-        out[k] = k;
-        if (out_sc) out_sc[k] = pr[k];
-      } else if (k >= tail_r) {
-        const int b = hi + (k - tail_r);
-        const bool real = b <= recent;
-        out[k] = real ? b : -1;
-        if (out_sc) out_sc[k] = real ? pr[b] : -INFINITY;
-      }
-    }
-    pdl_launch_dependents();
-    return;
-  }
-
   // this thread's candidate keys stay in registers across the passes (rows of
-  // up to kTopkThreads * kKeysPerThread candidates; longer rows re-read them)
+  // up to THREADS * kKeysPerThread candidates; longer rows re-read them)
   const int cnt = max(0, b1 - b0);
   const bool inreg = per <= kKeysPerThread;
   uint32_t keys[kKeysPerThread];
@@ -174,6 +142,93 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
   int need_eq = 0;
   const bool take_all = ncand <= kfree;
   const bool take_none = !take_all && kfree <= 0;
+
+  // ---------------- threshold + rank test
+  if (!take_all && !take_none && inreg && kfree <= 32) {
+    constexpr int L = THREADS / 32;  // threads per group (32 groups)
+    const int lane = threadIdx.x & 31;
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kKeysPerThread; ++i)
+      if (i < cnt) m = max(m, keys[i]);
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane % L == 0) gmax[threadIdx.x / L] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // rank of this group's maximum among the 32 (ties by group index)
+      const uint32_t mine = gmax[lane];
+      int rank = 0;
+#pragma unroll 8
+      for (int x = 0; x < 32; ++x) {
+        const uint32_t o = gmax[x];
+        rank += (o > mine) || (o == mine && x < lane);
+      }
+      if (rank == kfree - 1) sh_prefix = mine;
+    }
+    __syncthreads();
+    const uint32_t tq = sh_prefix;
+    int mine_c = 0;
+#pragma unroll
+    for (int i = 0; i < kKeysPerThread; ++i) mine_c += (i < cnt && keys[i] >= tq);
+    int cbase = 0;
+    const int C = block_exclusive_scan<THREADS>(mine_c, warp_tot, cbase);
+    if (C <= kCandMax) {  // block-uniform
+      uint32_t own_sel = 0;  // bit i: key i of this thread is a candidate
+      {
+        int c = cbase;
+#pragma unroll
+        for (int i = 0; i < kKeysPerThread; ++i)
+          if (i < cnt && keys[i] >= tq) {
+            ck[c++] = keys[i];
+            own_sel |= 1u << i;
+          }
+      }
+      __syncthreads();
+      // candidate e is kept iff fewer than kfree candidates beat it (a higher
+      // key, or the same key and a smaller id = a smaller index here)
+      for (int e = threadIdx.x; e < C; e += THREADS) {
+        const uint32_t ke = ck[e];
+        int beat = 0;
+        for (int x = 0; x < C; ++x) {
+          const uint32_t kx = ck[x];
+          beat += (kx > ke) || (kx == ke && x < e);
+        }
+        csel[e] = beat < kfree;
+      }
+      __syncthreads();
+      // this thread's kept ids, in order, at n_init + (kept candidates before them)
+      if (own_sel) {
+        int o = n_init;
+        for (int x = 0; x < cbase; ++x) o += csel[x];
+        int e = cbase;
+#pragma unroll
+        for (int i = 0; i < kKeysPerThread; ++i)
+          if (own_sel & (1u << i)) {
+            if (csel[e]) {
+              out[o] = b0 + i;
+              if (out_sc) out_sc[o] = pr[b0 + i];
+              ++o;
+            }
+            ++e;
+          }
+      }
+      const int tail_r = n_init + kfree;
+      for (int k = threadIdx.x; k < K; k += THREADS) {
+        if (k < n_init) {
+          out[k] = k;
+          if (out_sc) out_sc[k] = pr[k];
+        } else if (k >= tail_r) {
+          const int b = hi + (k - tail_r);
+          const bool real = b <= recent;
+          out[k] = real ? b : -1;
+          if (out_sc) out_sc[k] = real ? pr[b] : -INFINITY;
+        }
+      }
+      pdl_launch_dependents();
+      return;
+    }
+  }
   if (!take_all && !take_none) {
     uint32_t prefix = 0, pmask = 0;
     int remaining = kfree;
