@@ -146,7 +146,7 @@ struct Plan {
   bool direct = false;      // one query token: the attend reads the selection rows directly
   size_t off_status = 0, off_pooled = 0, off_uids = 0, off_umask = 0, off_ucount = 0, off_ctr = 0, off_qfa = 0,
          off_cfa = 0, off_po = 0, off_pml = 0, total = 0;
-  int nctr = 0;             // attend counters: [S*G] per (sequence, group) + 1 unit counter
+  int nctr = 0;             // attend counters: splits finished per (sequence, group)
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -174,19 +174,18 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   if (pl.ga.cols > kMaxAttendCols || pl.ga.nt * pl.ga.sp > 8) return MSA_ERR_UNSUPPORTED;
   pl.cap = Q * cfg->topk;
   pl.direct = (b->q_per_seq == 1);
-  // blocks per split: what one attend CTA keeps in flight
-  pl.bps = attend_stages(fa < 0 ? FMT_FP8 : fa, pl.ga.nt);
   // a union never holds more blocks than a sequence has
   const int cap_eff = pl.cap < b->max_blocks_per_seq ? pl.cap : b->max_blocks_per_seq;
+  pl.bps = attend_blocks_per_split(cap_eff, (long)S * G, 2 * sm_count());
   pl.splits = (cap_eff + pl.bps - 1) / pl.bps;
-  pl.nctr = 0;
+  pl.nctr = S * G;  // splits finished per (sequence, group)
   size_t o = 0;
   pl.off_status = o; o = align256(o + 256);
   pl.off_pooled = o; o = align256(o + (size_t)S * Q * G * b->max_blocks_per_seq * 4);
   pl.off_uids = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_umask = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_ucount = o; o = align256(o + (size_t)S * G * 4);
-  pl.off_ctr = o;
+  pl.off_ctr = o; o = align256(o + (size_t)pl.nctr * 4);
   pl.off_qfa = o; o = align256(o + (size_t)S * G * pl.ga.words_per_unit() * 4);
   pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
   pl.off_po = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 128 * 4);
@@ -286,9 +285,8 @@ msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, cons
   tp.topk_idx = topk_idx;
   tp.topk_score = topk_score;
   tp.status = pl ? at<DeviceStatus>(ws, pl->off_status) : static_cast<DeviceStatus*>(ws);
-  tp.zero = nullptr;
-  tp.nzero = 0;
-  (void)clear_ctr;
+  tp.zero = (clear_ctr && pl) ? at<int32_t>(ws, pl->off_ctr) : nullptr;  // for the attend that follows
+  tp.nzero = (clear_ctr && pl) ? pl->nctr : 0;
   tp.frag = nullptr;
   tp.colf = nullptr;
   if (frag_job && pl) set_frag_job(tp, frag_job->c, cfg, frag_job->q, frag_job->hq, *pl, ws);
@@ -313,8 +311,8 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   up.u_ids = at<int32_t>(ws, pl.off_uids);
   up.u_mask = at<uint32_t>(ws, pl.off_umask);
   up.u_count = at<int32_t>(ws, pl.off_ucount);
-  up.zero = nullptr;
-  up.nzero = 0;
+  up.zero = at<int32_t>(ws, pl.off_ctr);  // for the attend that follows
+  up.nzero = pl.nctr;
   set_frag_job(up, c, cfg, q, hq, pl, ws);
   up.status = status;
   if (!direct) {
@@ -359,31 +357,14 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   ap.bps = pl.bps;
   ap.splits = pl.splits;
   ap.work_ctr = nullptr;
-  ap.sg_ctr = nullptr;
+  ap.sg_ctr = at<int32_t>(ws, pl.off_ctr);
   ap.part_o = at<float>(ws, pl.off_po);
   ap.part_ml = at<float>(ws, pl.off_pml);
   ap.out = out;
   ap.lse = lse;
   ap.status = status;
   if (launch_attend(fa, tkp, tvp, ap, sm_count(), st, true) != cudaSuccess) return MSA_ERR_CUDA;
-  if (pl.splits == 1) return MSA_OK;  // every (sequence, group) fits one split: written by the attend
-  CombineParams cp;
-  cp.S = pl.S;
-  cp.Q = pl.Q;
-  cp.G = G;
-  cp.r = pl.r;
-  cp.splits = pl.splits;
-  cp.cols = pl.ga.cols;
-  cp.bps = pl.bps;
-  cp.topk = cfg->topk;
-  cp.direct = ap.direct;
-  cp.topk_idx = topk_idx;
-  cp.u_count = up.u_count;
-  cp.part_o = ap.part_o;
-  cp.part_ml = ap.part_ml;
-  cp.out = out;
-  cp.lse = lse;
-  return cuda_status(launch_combine(cp, st, true));
+  return MSA_OK;
 }
 
 }  // namespace

@@ -8,19 +8,24 @@
 // several new tokens per sequence (speculative verify, prefill chunks) each
 // token has its own selection and causal limit.
 //
-// Work.  Unit = (sequence, group, split): the group's selected blocks (for
+// Work.  Item = (sequence, group, split): the group's selected blocks (for
 // several query tokens: the union of their selections) cut into splits of
-// `bps` blocks, one CTA per unit, several CTAs per SM so that the hardware
-// overlaps one CTA's loads with another's math.  Warp 0 fetches the unit's
-// facts with parallel lane loads and thread 0 issues every block of the unit
-// at once (one shared-memory stage per block: TMA tensor copies with the
-// 128-byte swizzle for FP8 / BF16, bulk copies for NVFP4), together with the
-// query fragments the preceding kernel prepared.  Warp w owns keys
-// [32w, 32w+32) of every block with its own online softmax; at the end the
-// four warps merge through shared memory (over the dead stages).  A (sequence,
-// group) that fits one split writes its bf16 output and LSE directly;
-// otherwise each split writes a partial and combine_kernel merges them by
-// log-sum-exp (one warp per output row and head).
+// `bps` blocks.  The kernel is persistent: a grid of as many CTAs as fit on
+// the GPU walks the items with a static stride.  In each CTA one producer
+// warp reads the items' facts (block ids, query masks, physical blocks; the
+// counts of 32 items at once, so that empty splits cost nothing), publishes
+// them in one of two item slots together with a bulk copy of the query
+// fragments the preceding kernel prepared, and streams every block through a
+// ring of shared-memory stages (TMA tensor copies with the 128-byte swizzle
+// for FP8 / BF16, bulk copies for NVFP4), gated by per-stage full / empty
+// mbarriers.  Four consumer warps own keys [32w, 32w+32) of every block, each
+// with its own online softmax; at the end of an item they merge through a
+// dedicated shared-memory area (named barriers among the consumers only), so
+// the next item's copies keep streaming meanwhile.  A (sequence, group) that
+// fits one split writes its bf16 output and LSE directly; otherwise each split
+// writes a partial and combine_kernel merges them by log-sum-exp (one warp per
+// output row and head).  Every wait is bounded; a wait that gives up raises
+// the timeout flag and the CTA winds down without further copies.
 //
 // Tensor-core mapping, keys as MMA rows (the query side is only Q x r <= 32
 // columns wide):
@@ -40,9 +45,20 @@ namespace msa {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kWarps = 4;                 // consumer warps
+constexpr int kThreads = 32 * (kWarps + 1);  // + the producer warp
+constexpr int kConsumers = 32 * kWarps;
+constexpr int kMaxBps = kMaxBlocksPerSplit;  // blocks per split at most
 constexpr int kMergeRow = 132;  // padded row of the merge area (conflict-free stores)
+
+// What the producer publishes for one item.
+struct ItemFacts {
+  int32_t sg, split, n, count;  // n = -1: no more items
+  int32_t empty_sg, pad[3];
+  int32_t sb[kMaxBps];          // block ids (-1: rejected)
+  uint32_t smask[kMaxBps];      // query tokens that selected each block
+  int32_t sok[kMaxBps];         // 1: the block was copied
+};
 
 template <int FMT>
 struct AttTraits;
@@ -63,34 +79,39 @@ struct AttTraits<FMT_NVFP4> {
 };
 
 __host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-__host__ __device__ constexpr size_t cmax(size_t a, size_t b) { return a > b ? a : b; }
 
-// Blocks per unit (= stages): all of a unit's tiles are in flight at once.
-template <int FMT, int NT>
-__host__ __device__ constexpr int att_stages() {
-  return FMT == FMT_BF16 ? 2 : (FMT == FMT_FP8 ? 2 : (NT == 1 ? 4 : 2));
-}
-
-template <int FMT, int NT, int SP>
-struct AttLayout {
+template <int FMT, int NT, int SP, int NSTAGES>
+struct AttLayoutN {
   using T = AttTraits<FMT>;
   static constexpr int NC = NT * 8;
-  static constexpr int NST = att_stages<FMT, NT>();
+  static constexpr int NST = NSTAGES;
   static constexpr size_t TILES = (size_t)T::KTILE + T::VTILE + T::KSC + T::VSC;
   static constexpr size_t STAGE = round_up(TILES, 1024);
   static constexpr size_t FRAGW = (size_t)SP * NT * T::QKS * 64 * 4;  // query fragment words
-  static constexpr size_t FRAG_OFF = STAGE * NST;
   static constexpr size_t FRAG = FRAGW + NC * 4;                      // + column factors
-  static constexpr size_t PSM = round_up(FRAG_OFF + FRAG, 16);        // per-warp P tiles
+  static constexpr size_t ISLOT = round_up(FRAG, 128);
+  static constexpr size_t ITEM_OFF = STAGE * NST;                     // two item slots
+  static constexpr size_t PSM = ITEM_OFF + 2 * ISLOT;                 // per-warp P tiles
   static constexpr size_t PSM_WARP = 64 * NC;
   static constexpr size_t VDQ = PSM + kWarps * PSM_WARP;              // NVFP4 V^T f16 tiles
-  static constexpr size_t VDQ_WARP = (FMT == FMT_NVFP4) ? 32 * 256 : 0;
-  static constexpr size_t DATA_END = VDQ + kWarps * VDQ_WARP;
-  static constexpr size_t MERGE_BYTES = (size_t)kWarps * NC * (kMergeRow + 2) * 4;  // aliases the data area
-  static constexpr size_t BARS = round_up(cmax(DATA_END, MERGE_BYTES), 16);
-  static constexpr size_t TOTAL = BARS + 8 * NST + 8 + 16 * NST + 16;
+  static constexpr size_t VDQ_WARP = (FMT == FMT_NVFP4) ? 32 * 256 : 0;  // x 4 warps: one 128-row f16 V tile
+  static constexpr int KG = kWarps / NT;                              // warps sharing a column tile
+  static constexpr size_t MERGE = round_up(VDQ + kWarps * VDQ_WARP, 16);  // KG > 1: the warps' o, m, l
+  static constexpr size_t MERGE_BYTES = (KG > 1) ? (size_t)kWarps * 8 * (kMergeRow + 2) * 4 : 0;
+  static constexpr size_t FACTS = round_up(MERGE + MERGE_BYTES + 16, 16);
+  static constexpr size_t BARS = round_up(FACTS + 2 * sizeof(ItemFacts), 16);
+  static constexpr size_t TOTAL = BARS + 8 * (2 * NST + 4) + 16;
   static constexpr size_t SMEM = TOTAL + 1024;
 };
+
+// Ring depth: three stages where two CTAs still fit on an SM (228 KB of
+// shared memory, 1 KB of it reserved per CTA), else two.
+template <int FMT, int NT, int SP>
+constexpr int ring_stages() {
+  return 2 * (AttLayoutN<FMT, NT, SP, 3>::SMEM + 1024) <= 228 * 1024 ? 3 : 2;
+}
+template <int FMT, int NT, int SP>
+using AttLayout = AttLayoutN<FMT, NT, SP, ring_stages<FMT, NT, SP>()>;
 
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
   return base + row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -108,429 +129,295 @@ __device__ __forceinline__ void transpose4x4(const uint32_t in[4], uint32_t out[
   out[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// col / r for the small counts here (col < 4096, 1 <= r <= 64): the float
+// quotient of col + 1/2 lies at least 1/(2r) from an integer, far beyond its
+// rounding error, so the truncation is exact.
+__device__ __forceinline__ int col_div(int col, int r) {
+  return (int)(((float)col + 0.5f) * __frcp_rn((float)r));
+}
+
+// 2^e as a float for e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Largest e with v * 2^e <= 448 for a normal v > 0 (448 = 1.75 * 2^8), from
+// the exponent and mantissa fields; other v go the general way.
+__device__ __forceinline__ int fit448(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const int be = (int)((u >> 23) & 0xffu);
+  if (!(v > 0.f) || be == 0 || be == 255) return pow2_fit(v, 448.f);
+  const int E = be - 127;
+  return ((u & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;
+}
+
+// One block of keys for one consumer warp.  The four consumer warps split the
+// work as NT column tiles x (4 / NT) key ranges: warp w takes column tile
+// ct = w / (4 / NT) (8 query x head columns) and the KW = 32 * NT keys
+// starting at kw.  Logits for its keys, masked online softmax, P into its
+// shared tile, O^T += V^T P for its columns.
 template <int FMT, int NT, int SP>
-__global__ void __launch_bounds__(kThreads)
-    attend_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const AttendParams p) {
+__device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, uint8_t* vdq,
+                                             const uint32_t* __restrict__ fr, int ct, const float (&colf)[2],
+                                             const int (&qlim)[2], const int (&qbit)[2], uint32_t qmask, int key0,
+                                             int kw, int warp, int lane, float (&m_run)[2], float (&l_run)[2],
+                                             float (&o)[8][4], int& e_prev) {
   using TR = AttTraits<FMT>;
-  using LY = AttLayout<FMT, NT, SP>;
-  constexpr int NC = NT * 8;
-  constexpr int NST = LY::NST;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + LY::BARS);
-  uint64_t* fbar = full + NST;
-  int* sb = reinterpret_cast<int*>(fbar + 1);          // [NST] block ids
-  uint32_t* smask = reinterpret_cast<uint32_t*>(sb + NST);
-  int* sok = reinterpret_cast<int*>(smask + NST);      // [NST] 1: loaded
-  int* sinfo = sok + NST;                              // n, count, empty
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BatchDev bt = p.batch;
-  const int G = p.G, Q = bt.Q;
-  const int cols = p.geom.cols;
-  const int unit = blockIdx.x;
-  const int sg = unit / p.splits, split = unit % p.splits;
-  const int s = sg / G, g = sg % G;
-
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < NST; ++st) mbar_init(&full[st], 1);
-    mbar_init(fbar, 1);
-    fence_mbar_init();
-    if constexpr (FMT != FMT_NVFP4) {
-      prefetch_tmap(&tmk);
-      prefetch_tmap(&tmv);
-    }
-  }
-  pdl_wait();  // the selection / union, fragments and counters come from the preceding kernel
-  const int T = bt.seq_len(s);
-
-  // ---------------- warp 0: the unit's facts (parallel lane loads); thread 0 issues every copy
-  if (warp == 0) {
-    int entry = -1, count;
-    if (p.direct) {
-      entry = (lane < p.topk) ? p.topk_idx[(size_t)sg * p.topk + lane] : -1;
-      count = __popc(__ballot_sync(0xffffffffu, entry >= 0));
-    } else {
-      count = p.u_count[sg];
-    }
-    const int kb0 = split * p.bps;
-    int n = min(p.bps, count - kb0);
-    const bool empty_sg = (count == 0);
-    if (n < 0) n = 0;
-    int b = -1, phys = -1;
-    uint32_t mask = 0;
-    if (lane < n) {
-      if (p.direct) {
-        mask = 1u;
-      } else {
-        b = p.u_ids[(size_t)sg * p.cap + kb0 + lane];
-        mask = p.u_mask[(size_t)sg * p.cap + kb0 + lane];
-      }
-    }
-    if (p.direct) b = __shfl_sync(0xffffffffu, entry, (kb0 + lane) & 31);
-    if (lane < n) {
-      if (b < 0 || T < 0 || b > (T - 1) / kBlock) {
-        raise_flag(p.status, FLAG_BAD_SELECT, b);
-        b = -1;
-      } else {
-        const int ph = bt.row(s)[b];
-        if (ph < 0 || ph >= p.num_blocks) raise_flag(p.status, FLAG_BAD_BLOCK, ph);
-        else phys = ph;
-      }
-      sb[lane] = b;
-      smask[lane] = mask;
-      sok[lane] = phys >= 0 ? 1 : 0;
-    }
-    if (lane == 0) {
-      sinfo[0] = n;
-      sinfo[1] = count;
-      sinfo[2] = empty_sg ? 1 : 0;
-      if (n > 0) {
-        uint8_t* fd = base + LY::FRAG_OFF;
-        mbar_expect_tx(fbar, (uint32_t)LY::FRAG);
-        bulk_g2s(fd, p.frag + (size_t)sg * (LY::FRAGW / 4), (uint32_t)LY::FRAGW, fbar);
-        bulk_g2s(fd + LY::FRAGW, p.colf + (size_t)sg * NC, NC * 4, fbar);
-      }
-    }
-    for (int k = 0; k < n; ++k) {
-      const int ph = __shfl_sync(0xffffffffu, phys, k);
-      if (lane == 0 && ph >= 0) {
-        uint8_t* stg = base + (size_t)k * LY::STAGE;
-        const size_t tile_id = (size_t)ph * G + g;
-        mbar_expect_tx(&full[k], (uint32_t)LY::TILES);
-        if constexpr (FMT == FMT_FP8) {
-          tma_load_2d(stg, &tmk, 0, (int)(tile_id * kBlock), &full[k]);
-          tma_load_2d(stg + TR::KTILE, &tmv, 0, (int)(tile_id * kBlock), &full[k]);
-          bulk_g2s(stg + TR::KTILE + TR::VTILE, p.k_scale + tile_id * kBlock, TR::KSC, &full[k]);
-          bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_scale + tile_id * kBlock, TR::VSC, &full[k]);
-        } else if constexpr (FMT == FMT_BF16) {
-          tma_load_2d(stg, &tmk, 0, (int)(tile_id * kBlock), &full[k]);
-          tma_load_2d(stg + 128 * 128, &tmk, 64, (int)(tile_id * kBlock), &full[k]);
-          tma_load_2d(stg + TR::KTILE, &tmv, 0, (int)(tile_id * kBlock), &full[k]);
-          tma_load_2d(stg + TR::KTILE + 128 * 128, &tmv, 64, (int)(tile_id * kBlock), &full[k]);
-        } else {
-          bulk_g2s(stg, p.k + tile_id * TR::KTILE, TR::KTILE, &full[k]);
-          bulk_g2s(stg + TR::KTILE, p.v + tile_id * TR::VTILE, TR::VTILE, &full[k]);
-          bulk_g2s(stg + TR::KTILE + TR::VTILE, p.k_sf + tile_id * TR::KSC, TR::KSC, &full[k]);
-          bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_sf + tile_id * TR::VSC, TR::VSC, &full[k]);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  pdl_launch_dependents();
-  const int n = sinfo[0];
-  const int count = sinfo[1];
-  if (n == 0 && !(sinfo[2] && split == 0)) return;  // nothing in this split (the sequence's last splits)
-
-  // ---------------- every warp: query fragments, softmax state
+  constexpr int MT = 2 * NT;  // m tiles of 16 keys
+  constexpr int KW = 16 * MT; // keys of this warp
   const int g8 = lane >> 2, j = lane & 3;
-  const int kw = 32 * warp;  // this warp's keys within a block
-  uint8_t* psm = base + LY::PSM + (size_t)warp * LY::PSM_WARP;
-  uint32_t bq[SP][NT][TR::QKS][2];
-  float colf[NT][2];
-  int qlim[NT][2], qbit[NT][2];
-  float m_run[NT][2], l_run[NT][2];
-  float o[8][NT][4];
-  int e_prev = 0;
-  bool dead = false;
-  if (n > 0) {
-    if (!mbar_wait_warp(fbar, 0)) {
-      if (lane == 0) raise_flag(p.status, FLAG_TIMEOUT, unit);
-      dead = true;
-    }
-  }
-  if (n > 0 && !dead) {
-    const uint32_t* fr = reinterpret_cast<const uint32_t*>(base + LY::FRAG_OFF);
-    const float* cf = reinterpret_cast<const float*>(base + LY::FRAG_OFF + LY::FRAGW);
+  // query fragment word (term sp, k step ks, register rg) of this lane for column
+  // tile ct, read from the item's shared copy where it is used
+#define QF(sp, ks, rg) fr[((((sp) * NT + ct) * TR::QKS + (ks)) * 2 + (rg)) * 32 + lane]
+  // ---------------- logits^T for this warp's keys
+  float sacc[MT][4];
 #pragma unroll
-    for (int sp = 0; sp < SP; ++sp)
+  for (int mt = 0; mt < MT; ++mt) sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+  const uint32_t kt = smem_u32(stg);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+  for (int mt = 0; mt < MT; ++mt) {
+    if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
+      const int row = kw + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-        for (int ks = 0; ks < TR::QKS; ++ks)
+      for (int ks = 0; ks < TR::QKS; ++ks) {
+        uint32_t a[4];
+        if constexpr (FMT == FMT_FP8) {
+          ldmatrix_x4(a, swz(kt, row, 2 * ks + (lane >> 4)));
 #pragma unroll
-          for (int rg = 0; rg < 2; ++rg) bq[sp][nt][ks][rg] = fr[(((sp * NT + nt) * TR::QKS + ks) * 2 + rg) * 32 + lane];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) colf[nt][c] = cf[nt * 8 + 2 * j + c];
-  }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col = nt * 8 + 2 * j + c;
-      const int qi = col / p.r;
-      qlim[nt][c] = (col < cols) ? T - Q + qi : -1;
-      qbit[nt][c] = (col < cols) ? qi : 0;
-      m_run[nt][c] = -INFINITY;
-      l_run[nt][c] = 0.f;
-#pragma unroll
-      for (int mm = 0; mm < 8; ++mm) o[mm][nt][c] = o[mm][nt][c + 2] = 0.f;
-    }
-
-  for (int k = 0; k < n && !dead; ++k) {
-    if (!sok[k]) continue;  // rejected block: nothing was copied, nothing to wait for
-    if (!mbar_wait_warp(&full[k], 0)) {
-      if (lane == 0) raise_flag(p.status, FLAG_TIMEOUT, unit);
-      dead = true;
-      break;
-    }
-    const uint8_t* stg = base + (size_t)k * LY::STAGE;
-    const uint32_t qmask = smask[k];
-    const int key0 = sb[k] * kBlock + kw;
-    // ---------------- logits^T for this warp's 32 keys
-    float sacc[2][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sacc[mt][nt][0] = sacc[mt][nt][1] = sacc[mt][nt][2] = sacc[mt][nt][3] = 0.f;
-    const uint32_t kt = smem_u32(stg);
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
-        const int row = kw + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int ks = 0; ks < TR::QKS; ++ks) {
-          uint32_t a[4];
-          if constexpr (FMT == FMT_FP8) {
-            ldmatrix_x4(a, swz(kt, row, 2 * ks + (lane >> 4)));
-#pragma unroll
-            for (int sp = 0; sp < SP; ++sp)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_e4m3_k32(sacc[mt][nt], a, bq[sp][nt][ks][0], bq[sp][nt][ks][1]);
-          } else {
-            ldmatrix_x4(a, swz(kt + (ks >> 2) * (128 * 128), row, 2 * (ks & 3) + (lane >> 4)));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_k16(sacc[mt][nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
-          }
-        }
-      } else {
-        const int r0 = kw + 16 * mt + g8, r1 = r0 + 8;
-        const uint8_t* ksf = stg + TR::KTILE + TR::VTILE;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(stg + r0 * 64 + 16 * j);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(stg + r1 * 64 + 16 * j);
-        const uint16_t sc0 = *reinterpret_cast<const uint16_t*>(ksf + r0 * 8 + 2 * j);
-        const uint16_t sc1 = *reinterpret_cast<const uint16_t*>(ksf + r1 * 8 + 2 * j);
-        uint32_t s0[2], s1[2], h;
-        asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc0));
-        s0[0] = (h & 0xffffu) | (h << 16);
-        s0[1] = (h >> 16) | (h & 0xffff0000u);
-        asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc1));
-        s1[0] = (h & 0xffffu) | (h << 16);
-        s1[1] = (h >> 16) | (h & 0xffff0000u);
-        const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-        const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int ks = 0; ks < TR::QKS; ++ks) {
-          const int bi = 2 * ks;
-          const int grp = bi >> 3;
-          uint32_t x0 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
-          uint32_t x2 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
-          uint32_t x1 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
-          uint32_t x3 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
-          uint32_t a[4];
-          __half2 t;
-          t = __hmul2(*reinterpret_cast<__half2*>(&x0), *reinterpret_cast<const __half2*>(&s0[grp]));
-          a[0] = *reinterpret_cast<uint32_t*>(&t);
-          t = __hmul2(*reinterpret_cast<__half2*>(&x1), *reinterpret_cast<const __half2*>(&s1[grp]));
-          a[1] = *reinterpret_cast<uint32_t*>(&t);
-          t = __hmul2(*reinterpret_cast<__half2*>(&x2), *reinterpret_cast<const __half2*>(&s0[grp]));
-          a[2] = *reinterpret_cast<uint32_t*>(&t);
-          t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[grp]));
-          a[3] = *reinterpret_cast<uint32_t*>(&t);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_k16(sacc[mt][nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
+          for (int sp = 0; sp < SP; ++sp) mma_e4m3_k32(sacc[mt], a, QF(sp, ks, 0), QF(sp, ks, 1));
+        } else {
+          ldmatrix_x4(a, swz(kt + (ks >> 2) * (128 * 128), row, 2 * (ks & 3) + (lane >> 4)));
+          mma_bf16_k16(sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
         }
       }
-    }
-
-    // ---------------- scale, mask, online softmax (per column, over this warp's keys)
-    float ksc[2][2];
+    } else {
+      const int r0 = kw + 16 * mt + g8, r1 = r0 + 8;
+      const uint8_t* ksf = stg + TR::KTILE + TR::VTILE;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(stg + r0 * 64 + 16 * j);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(stg + r1 * 64 + 16 * j);
+      const uint16_t sc0 = *reinterpret_cast<const uint16_t*>(ksf + r0 * 8 + 2 * j);
+      const uint16_t sc1 = *reinterpret_cast<const uint16_t*>(ksf + r1 * 8 + 2 * j);
+      uint32_t s0[2], s1[2], h;
+      asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc0));
+      s0[0] = (h & 0xffffu) | (h << 16);
+      s0[1] = (h >> 16) | (h & 0xffff0000u);
+      asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "h"(sc1));
+      s1[0] = (h & 0xffffu) | (h << 16);
+      s1[1] = (h >> 16) | (h & 0xffff0000u);
+      const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+      const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+      for (int ks = 0; ks < TR::QKS; ++ks) {
+        const int bi = 2 * ks;
+        const int grp = bi >> 3;
+        uint32_t x0 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+        uint32_t x2 = e2m1x2_to_f16x2((wa[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+        uint32_t x1 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+        uint32_t x3 = e2m1x2_to_f16x2((wb[bi >> 2] >> (8 * ((bi + 1) & 3))) & 0xffu);
+        uint32_t a[4];
+        __half2 t;
+        t = __hmul2(*reinterpret_cast<__half2*>(&x0), *reinterpret_cast<const __half2*>(&s0[grp]));
+        a[0] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x1), *reinterpret_cast<const __half2*>(&s1[grp]));
+        a[1] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x2), *reinterpret_cast<const __half2*>(&s0[grp]));
+        a[2] = *reinterpret_cast<uint32_t*>(&t);
+        t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[grp]));
+        a[3] = *reinterpret_cast<uint32_t*>(&t);
+        mma_f16_k16(sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
+      }
+    }
+  }
+
+  // ---------------- scale, mask, online softmax (per column, over this warp's keys)
+  float ksc[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v = 1.f;
+      if constexpr (FMT == FMT_FP8)
+        v = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE)[kw + 16 * mt + g8 + 8 * hh];
+      ksc[mt][hh] = v;
+    }
+  float alpha[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const bool sel = (qmask >> qbit[c]) & 1u;
+    float bmax = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float v = 1.f;
-        if constexpr (FMT == FMT_FP8)
-          v = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE)[kw + 16 * mt + g8 + 8 * hh];
-        ksc[mt][hh] = v;
+        const int key = key0 + 16 * mt + g8 + 8 * hh;
+        const bool vis = sel && key <= qlim[c];
+        const float x = vis ? sacc[mt][c + 2 * hh] * ksc[mt][hh] * colf[c] : -INFINITY;
+        sacc[mt][c + 2 * hh] = x;
+        bmax = fmaxf(bmax, x);
       }
-    float alpha[NT][2];
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 4));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 8));
+    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
+    const float mnew = fmaxf(m_run[c], bmax);
+    const float msub = (mnew == -INFINITY) ? 0.f : mnew;
+    alpha[c] = ex2(m_run[c] - msub);
+    float psum = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const bool sel = (qmask >> qbit[nt][c]) & 1u;
-        float bmax = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int key = key0 + 16 * mt + g8 + 8 * hh;
-            const bool vis = sel && key <= qlim[nt][c];
-            const float x = vis ? sacc[mt][nt][c + 2 * hh] * ksc[mt][hh] * colf[nt][c] : -INFINITY;
-            sacc[mt][nt][c + 2 * hh] = x;
-            bmax = fmaxf(bmax, x);
-          }
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 4));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 8));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
-        const float mnew = fmaxf(m_run[nt][c], bmax);
-        const float msub = (mnew == -INFINITY) ? 0.f : mnew;
-        alpha[nt][c] = exp2f(m_run[nt][c] - msub);
-        float psum = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float pv = exp2f(sacc[mt][nt][c + 2 * hh] - msub);
-            sacc[mt][nt][c + 2 * hh] = pv;
-            psum += pv;
-          }
-        psum += __shfl_xor_sync(0xffffffffu, psum, 4);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 8);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 16);
-        l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + psum;
-        m_run[nt][c] = mnew;
+      for (int hh = 0; hh < 2; ++hh) {
+        const float pv = ex2(sacc[mt][c + 2 * hh] - msub);
+        sacc[mt][c + 2 * hh] = pv;
+        psum += pv;
       }
+    // per-lane partial row sum (this lane's keys); the 8 lanes of a column
+    // add theirs up once, at the merge
+    l_run[c] = l_run[c] * alpha[c] + psum;
+    m_run[c] = mnew;
+  }
 
-    // ---------------- P operand into this warp's shared tile, then B fragments
-    __syncwarp();
-    if constexpr (FMT == FMT_FP8) {
-      // P' = p * vscale * 2^e, split into e4m3 hi + lo
-      const float* vsc = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE + TR::KSC);
-      float vmax = vsc[kw + lane];
-      for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
-      const int e = pow2_fit(vmax, 448.f);
-      const float fe = ldexpf(1.f, e);
-      const float resc = ldexpf(1.f, e - e_prev);
-      e_prev = e;
-      // this lane's keys 16mt + g8 + 8hh of a column sit in bytes 2mt + hh of
-      // word g8 of that column's P row (keys j + 8i: bytes of b0, keys 4 + j + 8i:
-      // bytes of b1, for lane j): one word per (column, term)
+  // ---------------- P operand into this warp's shared tile
+  __syncwarp();
+  if constexpr (FMT == FMT_FP8) {
+    // P' = p * vscale * 2^e, split into e4m3 hi + lo; tile [term][column][KW bytes]
+    const float* vsc = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE + TR::KSC);
+    float vmax = vsc[kw + lane];
+#pragma unroll
+    for (int i = 1; i < NT; ++i) vmax = fmaxf(vmax, vsc[kw + 32 * i + lane]);
+    for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    const int e = min(126, fit448(vmax));
+    const float fe = (e >= -126) ? pow2i(e) : ldexpf(1.f, e);
+    const int de = e - e_prev;
+    const float resc = (de >= -126 && de <= 127) ? pow2i(de) : ldexpf(1.f, de);
+    e_prev = e;
+    // within each 32-key step, this lane's keys 16mt' + g8 + 8hh (mt' = 0, 1) sit in
+    // bytes 2mt' + hh of word g8 of the column's row (keys j + 8i: bytes of b0,
+    // keys 4 + j + 8i: bytes of b1, for lane j)
+    uint32_t* psm32 = reinterpret_cast<uint32_t*>(psm);
+#pragma unroll
+    for (int ks = 0; ks < NT; ++ks) {
       float vs[2][2];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int m2 = 0; m2 < 2; ++m2)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) vs[mt][hh] = vsc[kw + 16 * mt + g8 + 8 * hh] * fe;
-      uint32_t* psm32 = reinterpret_cast<uint32_t*>(psm);
+        for (int hh = 0; hh < 2; ++hh) vs[m2][hh] = vsc[kw + 32 * ks + 16 * m2 + g8 + 8 * hh] * fe;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int c = 0; c < 2; ++c) {
+        uint32_t hw = 0, lw = 0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float hi[4], lo[4];
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              split_e4m3(sacc[mt][nt][c + 2 * hh] * vs[mt][hh], hi[2 * mt + hh], lo[2 * mt + hh]);
-          const int col = nt * 8 + 2 * j + c;
-          psm32[col * 8 + g8] = (uint32_t)pack_e4m3x2(hi[0], hi[1]) | ((uint32_t)pack_e4m3x2(hi[2], hi[3]) << 16);
-          psm32[NC * 8 + col * 8 + g8] =
-              (uint32_t)pack_e4m3x2(lo[0], lo[1]) | ((uint32_t)pack_e4m3x2(lo[2], lo[3]) << 16);
+        for (int m2 = 0; m2 < 2; ++m2) {
+          const float x0 = sacc[2 * ks + m2][c] * vs[m2][0];
+          const float x1 = sacc[2 * ks + m2][c + 2] * vs[m2][1];
+          const uint16_t h = pack_e4m3x2(x0, x1);
+          const float2 hv = e4m3x2_to_float2(h);
+          const uint16_t l = pack_e4m3x2(x0 - hv.x, x1 - hv.y);
+          hw |= (uint32_t)h << (16 * m2);
+          lw |= (uint32_t)l << (16 * m2);
         }
-      // rescale the running output: softmax shift and the change of P scale
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const float f = alpha[nt][c] * resc;
-#pragma unroll
-          for (int mm = 0; mm < 8; ++mm) {
-            o[mm][nt][c] *= f;
-            o[mm][nt][c + 2] *= f;
-          }
-        }
-    } else {
-      // P as one 16-bit term: bf16 for BF16 tiles, f16 for NVFP4 tiles
-      uint16_t* ps16 = reinterpret_cast<uint16_t*>(psm);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int kk = 16 * mt + g8 + 8 * hh;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int col = nt * 8 + 2 * j + c;
-              const float pv = sacc[mt][nt][c + 2 * hh];
-              uint16_t bits;
-              if constexpr (FMT == FMT_BF16) {
-                __nv_bfloat16 x = __float2bfloat16_rn(pv);
-                bits = *reinterpret_cast<uint16_t*>(&x);
-              } else {
-                __half x = __float2half_rn(pv);
-                bits = *reinterpret_cast<uint16_t*>(&x);
-              }
-              ps16[col * 32 + kk] = bits;
-            }
-        }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int mm = 0; mm < 8; ++mm) {
-            o[mm][nt][c] *= alpha[nt][c];
-            o[mm][nt][c + 2] *= alpha[nt][c];
-          }
-      if constexpr (FMT == FMT_NVFP4) {
-        // dequantize this warp's 32 V rows to f16 (exact) into a swizzled tile
-        const uint8_t* vraw = stg + TR::KTILE;
-        const uint8_t* vsf = stg + TR::KTILE + TR::VTILE + TR::KSC;
-        uint8_t* vdq = base + LY::VDQ + (size_t)warp * LY::VDQ_WARP;
-        const int key = kw + lane;
-        const uint32_t vb = smem_u32(vdq);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 w = *reinterpret_cast<const uint4*>(vraw + key * 64 + 16 * q4);
-          const uint16_t scp = *reinterpret_cast<const uint16_t*>(vsf + key * 8 + 2 * q4);
-          uint32_t hsc;
-          asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(hsc) : "h"(scp));
-          const uint32_t sA = (hsc & 0xffffu) | (hsc << 16), sB = (hsc >> 16) | (hsc & 0xffff0000u);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          uint32_t out[16];
-#pragma unroll
-          for (int bi = 0; bi < 16; ++bi) {
-            uint32_t x = e2m1x2_to_f16x2((ww[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
-            __half2 t = __hmul2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(bi < 8 ? &sA : &sB));
-            out[bi] = *reinterpret_cast<uint32_t*>(&t);
-          }
-          // 32 dims = d 32*q4 .. +31 -> f16 bytes 64*q4 .. +63 -> half (q4>>1), chunks 4*(q4&1) .. +3
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t addr = swz(vb + (q4 >> 1) * (32 * 128), lane, 4 * (q4 & 1) + cc);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(out[4 * cc]), "r"(out[4 * cc + 1]),
-                         "r"(out[4 * cc + 2]), "r"(out[4 * cc + 3]));
-          }
-        }
+        const int col = 2 * j + c;
+        psm32[col * (KW / 4) + 8 * ks + g8] = hw;
+        psm32[8 * (KW / 4) + col * (KW / 4) + 8 * ks + g8] = lw;
       }
     }
-    __syncwarp();
-
-    // ---------------- O^T += V^T P
-    if constexpr (FMT == FMT_FP8) {
-      uint32_t bp[2][NT][2];
+    // rescale the running output: softmax shift and the change of P scale
 #pragma unroll
-      for (int sp = 0; sp < 2; ++sp)
+    for (int c = 0; c < 2; ++c) {
+      const float f = alpha[c] * resc;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint8_t* row = psm + sp * NC * 32 + (nt * 8 + g8) * 32;
-          bp[sp][nt][0] = *reinterpret_cast<const uint32_t*>(row + 4 * j);
-          bp[sp][nt][1] = *reinterpret_cast<const uint32_t*>(row + 16 + 4 * j);
+      for (int mm = 0; mm < 8; ++mm) {
+        o[mm][c] *= f;
+        o[mm][c + 2] *= f;
+      }
+    }
+  } else {
+    // P as one 16-bit term: bf16 for BF16 tiles, f16 for NVFP4 tiles; tile [column][KW]
+    uint16_t* ps16 = reinterpret_cast<uint16_t*>(psm);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int kk = 16 * mt + g8 + 8 * hh;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = 2 * j + c;
+          const float pv = sacc[mt][c + 2 * hh];
+          uint16_t bits;
+          if constexpr (FMT == FMT_BF16) {
+            __nv_bfloat16 x = __float2bfloat16_rn(pv);
+            bits = *reinterpret_cast<uint16_t*>(&x);
+          } else {
+            __half x = __float2half_rn(pv);
+            bits = *reinterpret_cast<uint16_t*>(&x);
+          }
+          ps16[col * KW + kk] = bits;
         }
-      const uint32_t vt = smem_u32(stg + TR::KTILE);
-      const int cg = (g8 >> 1) | ((g8 & 1) << 2);  // this lane's 16-dim chunk
+      }
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int mm = 0; mm < 8; ++mm) {
+        o[mm][c] *= alpha[c];
+        o[mm][c + 2] *= alpha[c];
+      }
+    if constexpr (FMT == FMT_NVFP4) {
+      // dequantize V rows 32w .. 32w+31 to f16 (exact) into the CTA's swizzled tile
+      const uint8_t* vraw = stg + TR::KTILE;
+      const uint8_t* vsf = stg + TR::KTILE + TR::VTILE + TR::KSC;
+      const int key = 32 * warp + lane;
+      const uint32_t vb = smem_u32(vdq);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 w = *reinterpret_cast<const uint4*>(vraw + key * 64 + 16 * q4);
+        const uint16_t scp = *reinterpret_cast<const uint16_t*>(vsf + key * 8 + 2 * q4);
+        uint32_t hsc;
+        asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(hsc) : "h"(scp));
+        const uint32_t sA = (hsc & 0xffffu) | (hsc << 16), sB = (hsc >> 16) | (hsc & 0xffff0000u);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        uint32_t out[16];
+#pragma unroll
+        for (int bi = 0; bi < 16; ++bi) {
+          uint32_t x = e2m1x2_to_f16x2((ww[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
+          __half2 t = __hmul2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(bi < 8 ? &sA : &sB));
+          out[bi] = *reinterpret_cast<uint32_t*>(&t);
+        }
+        // 32 dims = d 32*q4 .. +31 -> f16 bytes 64*q4 .. +63 -> half (q4>>1), chunks 4*(q4&1) .. +3
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t addr = swz(vb + (q4 >> 1) * (128 * 128), key, 4 * (q4 & 1) + cc);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(out[4 * cc]), "r"(out[4 * cc + 1]),
+                       "r"(out[4 * cc + 2]), "r"(out[4 * cc + 3]));
+        }
+      }
+      if constexpr (NT > 1) named_bar_sync(2, kConsumers);  // other warps' rows are read below
+    }
+  }
+  __syncwarp();
+
+  // ---------------- O^T += V^T P
+  if constexpr (FMT == FMT_FP8) {
+    const uint32_t vt = smem_u32(stg + TR::KTILE);
+    const int cg = (g8 >> 1) | ((g8 & 1) << 2);  // this lane's 16-dim chunk
+#pragma unroll
+    for (int ks = 0; ks < NT; ++ks) {
+      uint32_t bp[2][2];
+#pragma unroll
+      for (int sp = 0; sp < 2; ++sp) {
+        const uint8_t* row = psm + sp * 8 * KW + g8 * KW + 32 * ks;
+        bp[sp][0] = *reinterpret_cast<const uint32_t*>(row + 4 * j);
+        bp[sp][1] = *reinterpret_cast<const uint32_t*>(row + 16 + 4 * j);
+      }
       uint32_t A0[16], A2[16];
 #pragma unroll
       for (int set = 0; set < 2; ++set) {
         uint4 raw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int key = kw + 8 * i + 4 * set + j;
+          const int key = kw + 32 * ks + 8 * i + 4 * set + j;
           const uint32_t addr = swz(vt, key, cg);
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(raw[i].x), "=r"(raw[i].y), "=r"(raw[i].z), "=r"(raw[i].w)
@@ -541,200 +428,545 @@ __global__ void __launch_bounds__(kThreads)
         for (int wd = 0; wd < 4; ++wd) {
           uint32_t in[4], out[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) in[i] = (wd == 0) ? raw[i].x : (wd == 1) ? raw[i].y : (wd == 2) ? raw[i].z : raw[i].w;
+          for (int i = 0; i < 4; ++i)
+            in[i] = (wd == 0) ? raw[i].x : (wd == 1) ? raw[i].y : (wd == 2) ? raw[i].z : raw[i].w;
           transpose4x4(in, out);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) A[4 * wd + e] = out[e];
+          for (int e2 = 0; e2 < 4; ++e2) A[4 * wd + e2] = out[e2];
         }
       }
 #pragma unroll
       for (int mm = 0; mm < 8; ++mm) {
         const uint32_t a[4] = {A0[2 * mm], A0[2 * mm + 1], A2[2 * mm], A2[2 * mm + 1]};
+        mma_e4m3_k32(o[mm], a, bp[0][0], bp[0][1]);
+        mma_e4m3_k32(o[mm], a, bp[1][0], bp[1][1]);
+      }
+    }
+  } else {
+    const uint16_t* ps16 = reinterpret_cast<const uint16_t*>(psm);
+    const uint32_t vt = (FMT == FMT_BF16) ? smem_u32(stg + TR::KTILE) : smem_u32(vdq);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_e4m3_k32(o[mm][nt], a, bp[0][nt][0], bp[0][nt][1]);
-          mma_e4m3_k32(o[mm][nt], a, bp[1][nt][0], bp[1][nt][1]);
+    for (int kk = 0; kk < KW / 16; ++kk) {
+      const uint16_t* row = ps16 + g8 * KW + 16 * kk;
+      const uint32_t bp0 = *reinterpret_cast<const uint32_t*>(row + 2 * j);
+      const uint32_t bp1 = *reinterpret_cast<const uint32_t*>(row + 8 + 2 * j);
+      const int key = kw + 16 * kk + (lane & 7) + 8 * ((lane >> 4) & 1);
+#pragma unroll
+      for (int mm = 0; mm < 8; ++mm) {
+        const int d0 = 16 * mm + 8 * ((lane >> 3) & 1);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, swz(vt + (d0 >> 6) * (128 * 128), key, (d0 & 63) >> 3));
+        if constexpr (FMT == FMT_BF16)
+          mma_bf16_k16(o[mm], a, bp0, bp1);
+        else
+          mma_f16_k16(o[mm], a, bp0, bp1);
+      }
+    }
+    if constexpr (FMT == FMT_NVFP4 && NT > 1) named_bar_sync(2, kConsumers);  // before the tile is rewritten
+  }
+  __syncwarp();
+}
+
+#undef QF
+
+__device__ __forceinline__ bool cta_dead(const int* flag) { return *reinterpret_cast<const volatile int*>(flag) != 0; }
+
+__device__ __forceinline__ void set_dead(int* flag, DeviceStatus* st, int detail) {
+  if (!cta_dead(flag)) raise_flag(st, FLAG_TIMEOUT, detail);
+  *reinterpret_cast<volatile int*>(flag) = 1;
+}
+
+// Bounded warp-uniform wait that gives up at once when the CTA is winding down.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const int* dead) {
+  if (cta_dead(dead)) return false;
+  return mbar_wait_warp(bar, parity);
+}
+
+template <int FMT, int NT, int SP>
+__device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttendParams& p,
+                                                uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* ifull,
+                                                uint64_t* iempty, int* dead, ItemFacts* facts, int lane) {
+  using TR = AttTraits<FMT>;
+  using LY = AttLayout<FMT, NT, SP>;
+  constexpr int NC = NT * 8;
+  constexpr int NST = LY::NST;
+  const BatchDev bt = p.batch;
+  const int G = p.G;
+  const long items = (long)bt.S * G * p.splits;
+  const long stride = gridDim.x;
+  long bi = 0;  // blocks pushed through the ring
+  long ii = 0;  // items published
+  bool ok = true;
+  bool waited = false;
+  for (long it0 = blockIdx.x; it0 < items && ok; it0 += 32 * stride) {
+    // selected-block counts of the next 32 items of this CTA, one per lane.  One
+    // query token: the top-k keeps min(k, visible blocks) blocks, known from the
+    // sequence length alone (a caller input, readable before the wait).
+    const long my_it = it0 + lane * stride;
+    int my_cnt = 0;
+    if (p.direct && my_it < items) {
+      const int T = bt.seq_len((int)(my_it / p.splits) / G);
+      my_cnt = (T < 1 || T > bt.max_nb * kBlock) ? 0 : min(p.topk, (T - 1) / kBlock + 1);
+    }
+    if (!waited) {
+      pdl_wait();  // the selection / union and the query fragments come from the preceding kernel
+      waited = true;
+    }
+    if (!p.direct && my_it < items) my_cnt = p.u_count[(int)(my_it / p.splits)];
+    for (int t = 0; t < 32 && ok; ++t) {
+      const long it = it0 + t * stride;
+      if (it >= items) break;
+      const int count = __shfl_sync(0xffffffffu, my_cnt, t);
+      const int sg = (int)(it / p.splits), split = (int)(it % p.splits);
+      const int kb0 = split * p.bps;
+      const int n = max(0, min(p.bps, count - kb0));
+      const bool empty_sg = count <= 0;
+      if (n == 0 && !(empty_sg && split == 0)) continue;  // nothing in this split
+      const int s = sg / G, g = sg % G;
+      const int T = bt.seq_len(s);
+      int b = -1, phys = -1;
+      uint32_t mask = 0;
+      if (lane < n) {
+        if (p.direct) {
+          b = p.topk_idx[(size_t)sg * p.topk + kb0 + lane];
+          mask = 1u;
+        } else {
+          b = p.u_ids[(size_t)sg * p.cap + kb0 + lane];
+          mask = p.u_mask[(size_t)sg * p.cap + kb0 + lane];
+        }
+        if (b < 0 || T < 0 || b > (T - 1) / kBlock) {
+          raise_flag(p.status, FLAG_BAD_SELECT, b);
+          b = -1;
+        } else {
+          const int ph = bt.row(s)[b];
+          if (ph < 0 || ph >= p.num_blocks) raise_flag(p.status, FLAG_BAD_BLOCK, ph);
+          else phys = ph;
         }
       }
-    } else {
-      const uint16_t* ps16 = reinterpret_cast<const uint16_t*>(psm);
-      uint32_t vt;
-      int vrow0;
-      if constexpr (FMT == FMT_BF16) {
-        vt = smem_u32(stg + TR::KTILE);
-        vrow0 = kw;
-      } else {
-        vt = smem_u32(base + LY::VDQ + (size_t)warp * LY::VDQ_WARP);
-        vrow0 = 0;
+      // publish the item
+      const int slot = (int)(ii & 1);
+      const long use = ii >> 1;
+      if (use > 0 && !ring_wait(&iempty[slot], (uint32_t)((use - 1) & 1), dead)) {
+        set_dead(dead, p.status, (int)it);
+        ok = false;
+        break;
       }
-      constexpr int HALF = (FMT == FMT_BF16) ? 128 * 128 : 32 * 128;
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t bp[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint16_t* row = ps16 + (nt * 8 + g8) * 32 + 16 * kk;
-          bp[nt][0] = *reinterpret_cast<const uint32_t*>(row + 2 * j);
-          bp[nt][1] = *reinterpret_cast<const uint32_t*>(row + 8 + 2 * j);
+      ItemFacts& f = facts[slot];
+      if (lane < n) {
+        f.sb[lane] = b;
+        f.smask[lane] = mask;
+        f.sok[lane] = phys >= 0 ? 1 : 0;
+      }
+      if (lane == 0) {
+        f.sg = sg;
+        f.split = split;
+        f.n = n;
+        f.count = count;
+        f.empty_sg = empty_sg ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (n > 0) {
+          uint8_t* fd = base + LY::ITEM_OFF + (size_t)slot * LY::ISLOT;
+          fence_proxy_async();
+          mbar_expect_tx(&ifull[slot], (uint32_t)LY::FRAG);
+          bulk_g2s(fd, p.frag + (size_t)sg * (LY::FRAGW / 4), (uint32_t)LY::FRAGW, &ifull[slot]);
+          bulk_g2s(fd + LY::FRAGW, p.colf + (size_t)sg * NC, NC * 4, &ifull[slot]);
+        } else {
+          mbar_arrive(&ifull[slot]);
         }
-        const int key = vrow0 + 16 * kk + (lane & 7) + 8 * ((lane >> 4) & 1);
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) {
-          const int d0 = 16 * mm + 8 * ((lane >> 3) & 1);
-          uint32_t a[4];
-          ldmatrix_x4_trans(a, swz(vt + (d0 >> 6) * HALF, key, (d0 & 63) >> 3));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if constexpr (FMT == FMT_BF16)
-              mma_bf16_k16(o[mm][nt], a, bp[nt][0], bp[nt][1]);
-            else
-              mma_f16_k16(o[mm][nt], a, bp[nt][0], bp[nt][1]);
+      }
+      ++ii;
+      // its blocks, through the ring
+      for (int k = 0; k < n; ++k) {
+        const int ph = __shfl_sync(0xffffffffu, phys, k);
+        const int st = (int)(bi % NST);
+        const long ub = bi / NST;
+        if (ub > 0 && !ring_wait(&empty[st], (uint32_t)((ub - 1) & 1), dead)) {
+          set_dead(dead, p.status, (int)it);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (ph >= 0) {
+            uint8_t* stg = base + (size_t)st * LY::STAGE;
+            const size_t tile_id = (size_t)ph * G + g;
+            fence_proxy_async();
+            mbar_expect_tx(&full[st], (uint32_t)LY::TILES);
+            if constexpr (FMT == FMT_FP8) {
+              tma_load_2d(stg, tmk, 0, (int)(tile_id * kBlock), &full[st]);
+              tma_load_2d(stg + TR::KTILE, tmv, 0, (int)(tile_id * kBlock), &full[st]);
+              bulk_g2s(stg + TR::KTILE + TR::VTILE, p.k_scale + tile_id * kBlock, TR::KSC, &full[st]);
+              bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_scale + tile_id * kBlock, TR::VSC, &full[st]);
+            } else if constexpr (FMT == FMT_BF16) {
+              tma_load_2d(stg, tmk, 0, (int)(tile_id * kBlock), &full[st]);
+              tma_load_2d(stg + 128 * 128, tmk, 64, (int)(tile_id * kBlock), &full[st]);
+              tma_load_2d(stg + TR::KTILE, tmv, 0, (int)(tile_id * kBlock), &full[st]);
+              tma_load_2d(stg + TR::KTILE + 128 * 128, tmv, 64, (int)(tile_id * kBlock), &full[st]);
+            } else {
+              bulk_g2s(stg, p.k + tile_id * TR::KTILE, TR::KTILE, &full[st]);
+              bulk_g2s(stg + TR::KTILE, p.v + tile_id * TR::VTILE, TR::VTILE, &full[st]);
+              bulk_g2s(stg + TR::KTILE + TR::VTILE, p.k_sf + tile_id * TR::KSC, TR::KSC, &full[st]);
+              bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_sf + tile_id * TR::VSC, TR::VSC, &full[st]);
+            }
+          } else {
+            mbar_arrive(&full[st]);  // rejected block: an empty phase keeps the ring in step
           }
         }
+        ++bi;
       }
     }
-    __syncwarp();
   }
-
-  // ---------------- merge the four warps (over the dead stages), write output or partial
-  const bool any_dead = __syncthreads_or(dead);
-  if (any_dead) {
-    if (threadIdx.x == 0) {  // bounded wait for copies still in flight before their buffers are reused
-      mbar_wait(fbar, 0, 2000);
-      for (int k = 0; k < n; ++k)
-        if (sok[k]) mbar_wait(&full[k], 0, 2000);
+  if (!waited) pdl_wait();
+  // end of the stream
+  if (ok) {
+    const int slot = (int)(ii & 1);
+    const long use = ii >> 1;
+    if (use > 0 && !ring_wait(&iempty[slot], (uint32_t)((use - 1) & 1), dead)) {
+      set_dead(dead, p.status, -1);
+    } else if (lane == 0) {
+      facts[slot].n = -1;
+      mbar_arrive(&ifull[slot]);
     }
-    __syncthreads();
+    ++ii;
   }
-  float* om = reinterpret_cast<float*>(base);                 // [4][NC][kMergeRow], slot 16mm+8hh+g8
-  float* mls = om + (size_t)kWarps * NC * kMergeRow;          // [4][NC][2]
-  const float oscale = (FMT == FMT_FP8) ? ldexpf(1.f, -e_prev) : ((FMT == FMT_NVFP4) ? p.v_global : 1.f);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col = nt * 8 + 2 * j + c;
-      if (g8 == 0) {
-        mls[(warp * NC + col) * 2] = dead ? -INFINITY : m_run[nt][c];
-        mls[(warp * NC + col) * 2 + 1] = dead ? 0.f : l_run[nt][c];
-      }
-#pragma unroll
-      for (int mm = 0; mm < 8; ++mm)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          om[(warp * NC + col) * kMergeRow + 16 * mm + 8 * hh + g8] = o[mm][nt][c + 2 * hh] * oscale;
+  // before exiting, let the last copy into every stage and item slot land
+  // (immediate in a healthy run: the consumers waited for all of them)
+  if (lane == 0) {
+    for (int st = 0; st < NST; ++st) {
+      const long uses = bi > st ? (bi - 1 - st) / NST + 1 : 0;
+      if (uses > 0) mbar_wait(&full[st], (uint32_t)((uses - 1) & 1), 2000);
     }
-  __syncthreads();
-  const bool whole = (count <= p.bps);  // the (sequence, group) fits this one split
-  const int H = G * p.r;
-  float* po = p.part_o + (size_t)unit * cols * 128;
-  float* pml = p.part_ml + (size_t)unit * cols * 2;
-  for (int idx = threadIdx.x; idx < cols * 128; idx += kThreads) {
-    const int col = idx >> 7, d = idx & 127;
-    int slot;  // merge-area position of output dim d (inverse of the accumulator row mapping)
-    if constexpr (FMT == FMT_FP8) {
-      const int cgd = d >> 4;
-      const int g8d = ((cgd & 3) << 1) | (cgd >> 2);
-      slot = 16 * ((d & 15) >> 1) + 8 * (d & 1) + g8d;
-    } else {
-      slot = d;
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mls[(w * NC + col) * 2]);
-    float acc = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = mls[(w * NC + col) * 2];
-        const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        acc += f * om[(w * NC + col) * kMergeRow + slot];
-        L += f * mls[(w * NC + col) * 2 + 1];
-      }
-    }
-    if (whole) {
-      const int qi = col / p.r, hh = col % p.r;
-      const size_t orow = (size_t)(s * Q + qi) * H + g * p.r + hh;
-      static_cast<__nv_bfloat16*>(p.out)[orow * 128 + d] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
-      if (d == 0 && p.lse) p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    } else {
-      po[idx] = acc;
-      if (d == 0) {
-        pml[2 * col] = M;
-        pml[2 * col + 1] = L;
-      }
+    for (int sl = 0; sl < 2; ++sl) {
+      const long uses = ii > sl ? (ii - 1 - sl) / 2 + 1 : 0;
+      if (uses > 0) mbar_wait(&ifull[sl], (uint32_t)((uses - 1) & 1), 2000);
     }
   }
 }
 
-// out[row][h] = sum_k 2^(M_k - M) O_k / sum_k 2^(M_k - M) L_k over the splits of
-// its (sequence, group); rows whose (sequence, group) fit one split were
-// written by the attend itself.  One warp per (row, head); the loads of the
-// partials are independent so they overlap.
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
-  pdl_wait();
-  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int H = p.G * p.r;
-  if (wg >= p.S * p.Q * H) return;
-  const int h = wg % H, sq = wg / H;
-  const int s = sq / p.Q, i = sq % p.Q;
-  const int g = h / p.r, hh = h % p.r;
-  const int sg = s * p.G + g;
-  int count;
-  if (p.direct) {
-    const int e = (lane < p.topk) ? p.topk_idx[(size_t)sg * p.topk + lane] : -1;
-    count = __popc(__ballot_sync(0xffffffffu, e >= 0));
-  } else {
-    count = p.u_count[sg];
-  }
-  if (count <= p.bps) return;  // written by the attend
-  const int nparts = (count + p.bps - 1) / p.bps;
-  const int col = i * p.r + hh;
-  const size_t ubase = (size_t)sg * p.splits;
-  float M = -INFINITY;
-  for (int k0 = 0; k0 < nparts; k0 += 32) {
-    const int k = k0 + lane;
-    const float mk = (k < nparts) ? __ldcg(p.part_ml + ((ubase + k) * p.cols + col) * 2) : -INFINITY;
-    M = fmaxf(M, mk);
-  }
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int k0 = 0; k0 < nparts; k0 += 32) {
-      const int k = k0 + lane;
-      float f = 0.f, lk = 0.f;
-      if (k < nparts) {
-        const float mk = __ldcg(p.part_ml + ((ubase + k) * p.cols + col) * 2);
-        lk = __ldcg(p.part_ml + ((ubase + k) * p.cols + col) * 2 + 1);
-        f = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+// Atomic add at GPU scope with acquire-release semantics: the caller's earlier
+// writes (and those its CTA barrier ordered before it) are visible to whoever
+// reads the new count, and the old count it returns orders its later reads.
+__device__ __forceinline__ int atomic_add_acq_rel(int* a, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+
+// Merge of every split of one (sequence, group), by the CTA whose split
+// finished last: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.  One
+// thread per 4 output dims of a column; the splits are read 8 at a time with
+// every load of a group in flight together (one round trip per group).
+__device__ __noinline__ void merge_splits(const AttendParams& p, int sg, int nparts, int tid, bool write) {
+  const int G = p.G, Q = p.batch.Q, cols = p.geom.cols, H = G * p.r;
+  const int s = sg / G, g = sg % G;
+  const size_t pbase = (size_t)sg * p.splits;
+  for (int e = tid; e < cols * 32; e += kConsumers) {
+    const int col = e >> 5, d4 = (e & 31) * 4;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < nparts; i0 += 8) {
+      float mi[8], li[8];
+      float4 oi[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const size_t part = pbase + i0 + t;
+        const bool ok = i0 + t < nparts;
+        mi[t] = ok ? __ldcg(p.part_ml + (part * cols + col) * 2) : -INFINITY;
+        li[t] = ok ? __ldcg(p.part_ml + (part * cols + col) * 2 + 1) : 0.f;
+        oi[t] = ok ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (part * cols + col) * 128 + d4))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      float fl = f * lk;
-      for (int o = 16; o > 0; o >>= 1) fl += __shfl_xor_sync(0xffffffffu, fl, o);
-      L += fl;
-      const int kn = min(32, nparts - k0);
-#pragma unroll 8
-      for (int t = 0; t < kn; ++t) {
-        const float ft = __shfl_sync(0xffffffffu, f, t);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((ubase + k0 + t) * p.cols + col) * 128) + lane);
-        acc.x += ft * v.x;
-        acc.y += ft * v.y;
-        acc.z += ft * v.z;
-        acc.w += ft * v.w;
+      float mn = M;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mn = fmaxf(mn, mi[t]);
+      if (mn == -INFINITY) continue;
+      const float a = ex2(M - mn);  // M = -inf: 0
+      acc.x *= a;
+      acc.y *= a;
+      acc.z *= a;
+      acc.w *= a;
+      L *= a;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float w = ex2(mi[t] - mn);  // -inf: 0
+        acc.x += w * oi[t].x;
+        acc.y += w * oi[t].y;
+        acc.z += w * oi[t].z;
+        acc.w += w * oi[t].w;
+        L += w * li[t];
+      }
+      M = mn;
+    }
+    const float inv = (L > 0.f) ? __fdividef(1.f, L) : 0.f;
+    if (!write) continue;
+    const int qi = col_div(col, p.r), hh = col - qi * p.r;
+    const size_t orow = (size_t)(s * Q + qi) * H + g * p.r + hh;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow * 128 + d4) = pk;
+    if (d4 == 0 && p.lse) p.lse[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+template <int FMT, int NT, int SP>
+__device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* base, uint64_t* full, uint64_t* empty,
+                                                uint64_t* ifull, uint64_t* iempty, int* dead, const ItemFacts* facts,
+                                                int warp, int lane) {
+  using LY = AttLayout<FMT, NT, SP>;
+  constexpr int NST = LY::NST;
+  constexpr int KG = LY::KG;       // warps sharing a column tile (key ranges)
+  constexpr int KW = 32 * NT;      // keys of a warp
+  const BatchDev bt = p.batch;
+  const int G = p.G, Q = bt.Q;
+  const int cols = p.geom.cols;
+  const int H = G * p.r;
+  const int g8 = lane >> 2, j = lane & 3;
+  const int ct = warp / KG;         // this warp's column tile
+  const int kw = (warp % KG) * KW;  // and its keys within a block
+  const int tid = warp * 32 + lane;
+  uint8_t* psm = base + LY::PSM + (size_t)warp * LY::PSM_WARP;
+  uint8_t* vdq = base + LY::VDQ;
+  float* om = reinterpret_cast<float*>(base + LY::MERGE);  // KG > 1: [4 warps][8 cols][kMergeRow]
+  float* mls = om + (size_t)kWarps * 8 * kMergeRow;        // [4][8][2]: running max, row sum
+  int* last_flag = reinterpret_cast<int*>(base + LY::MERGE + LY::MERGE_BYTES);
+  long bi = 0;
+  int pend_sg = -1, pend_np = 0, pend_old = 0;  // the previous item's split count (answer in thread 0)
+  // Item -1 is a dry run before the grid dependency wait: the same code over
+  // the first stage with every key masked and no global writes, so that the
+  // instruction path is fetched while the preceding kernel still runs.
+  for (long ii = -1;; ++ii) {
+    const bool dry = ii < 0;
+    const int slot = dry ? 0 : (int)(ii & 1);
+    bool got = true;
+    if (!dry) {
+      got = ring_wait(&ifull[slot], (uint32_t)((ii >> 1) & 1), dead);
+      if (!got) set_dead(dead, p.status, (int)ii);
+    }
+    if (named_bar_or(1, kConsumers, !got)) break;  // every consumer warp leaves together
+    const ItemFacts& f = facts[slot];
+    const int n = dry ? 1 : f.n;
+    if (n < 0) break;
+    const int sg = dry ? 0 : f.sg, split = dry ? 0 : f.split, count = dry ? 0 : f.count;
+    const int s = sg / G, g = sg % G;
+    const int T = dry ? 0 : bt.seq_len(s);
+    const uint32_t* fr = reinterpret_cast<const uint32_t*>(base + LY::ITEM_OFF + (size_t)slot * LY::ISLOT);
+    const float* cf = reinterpret_cast<const float*>(base + LY::ITEM_OFF + (size_t)slot * LY::ISLOT + LY::FRAGW);
+
+    float colf[2], m_run[2], l_run[2];
+    int qlim[2], qbit[2];
+    float o[8][4];
+    int e_prev = 0;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int col = ct * 8 + 2 * j + c;
+      const int qi = col_div(col, p.r);
+      colf[c] = (n > 0) ? cf[col] : 0.f;
+      qlim[c] = (col < cols) ? T - Q + qi : -1;
+      qbit[c] = (col < cols) ? qi : 0;
+      m_run[c] = -INFINITY;
+      l_run[c] = 0.f;
+#pragma unroll
+      for (int mm = 0; mm < 8; ++mm) o[mm][c] = o[mm][c + 2] = 0.f;
+    }
+
+    for (int k = 0; k < n; ++k) {
+      const int st = dry ? 0 : (int)(bi % NST);
+      bool have = true;
+      if (!dry) {
+        have = ring_wait(&full[st], (uint32_t)((bi / NST) & 1), dead);
+        ++bi;
+        if (!have) set_dead(dead, p.status, sg);
+      }
+      if constexpr (FMT == FMT_NVFP4 && NT > 1) {
+        // the block's work has barriers among the consumers: decide together
+        have = !named_bar_or(1, kConsumers, !have);
+      }
+      if (have && (dry || f.sok[k])) {
+        attend_block<FMT, NT, SP>(base + (size_t)st * LY::STAGE, psm, vdq, fr, ct, colf, qlim, qbit,
+                                  dry ? 0u : f.smask[k], (dry ? 0 : f.sb[k]) * kBlock + kw, kw, warp, lane, m_run,
+                                  l_run, o, e_prev);
+      }
+      __syncwarp();
+      if (!dry && lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // ---------------- the item's result: its output rows when the (sequence, group)
+    // fits this split, else its partial (o, m, l), merged by the last split
+    const bool wdead = cta_dead(dead);
+    const float oscale = (FMT == FMT_FP8) ? (e_prev >= -126 && e_prev <= 126 ? pow2i(-e_prev) : ldexpf(1.f, -e_prev))
+                                           : ((FMT == FMT_NVFP4) ? p.v_global : 1.f);
+    const bool whole = (count <= p.bps);
+    const bool write = !dry;
+    const size_t part = (size_t)sg * p.splits + split;
+    float* po = p.part_o + part * cols * 128;
+    float* pml = p.part_ml + part * cols * 2;
+    float lsum[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float v = l_run[c];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      lsum[c] = v;
+    }
+    if constexpr (KG == 1) {
+      // this warp alone holds its columns: write them
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float M = wdead ? -INFINITY : m_run[c];
+        const float L = wdead ? 0.f : lsum[c];
+        const int col = ct * 8 + 2 * j + c;
+        if (col >= cols || !write) continue;
+        const float fo = whole ? (L > 0.f ? __fdividef(oscale, L) : 0.f) : oscale;
+        const int qi = col_div(col, p.r), hh = col - qi * p.r;
+        const size_t orow = (size_t)(s * Q + qi) * H + g * p.r + hh;
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            int d;  // accumulator row 16mm + 8h2 + g8 -> output dim
+            if constexpr (FMT == FMT_FP8) d = 16 * (((g8 & 1) << 2) | (g8 >> 1)) + 2 * mm + h2;
+            else d = 16 * mm + 8 * h2 + g8;
+            const float v = wdead ? 0.f : o[mm][c + 2 * h2] * fo;
+            if (whole) static_cast<__nv_bfloat16*>(p.out)[orow * 128 + d] = __float2bfloat16_rn(v);
+            else po[col * 128 + d] = v;
+          }
+        if (g8 == 0) {
+          if (whole) {
+            if (p.lse) p.lse[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+          } else {
+            pml[2 * col] = M;
+            pml[2 * col + 1] = L;
+          }
+        }
+      }
+    } else {
+      // the KG warps of a column tile hold different keys: merge them in shared memory
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int cl = 2 * j + c;
+        if (g8 == 0) {
+          mls[(warp * 8 + cl) * 2] = wdead ? -INFINITY : m_run[c];
+          mls[(warp * 8 + cl) * 2 + 1] = wdead ? 0.f : lsum[c];
+        }
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2)
+            om[(warp * 8 + cl) * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
+      }
+      named_bar_sync(1, kConsumers);
+      for (int e = tid; e < NT * 8 * 128; e += kConsumers) {
+        const int tct = e >> 10, cl = (e >> 7) & 7, sl = e & 127;  // tile, column, accumulator row
+        const int col = tct * 8 + cl;
+        if (col >= cols) continue;
+        int d;
+        if constexpr (FMT == FMT_FP8) {
+          const int g8s = sl & 7;
+          d = 16 * (((g8s & 1) << 2) | (g8s >> 1)) + 2 * (sl >> 4) + ((sl >> 3) & 1);
+        } else {
+          d = sl;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int kq = 0; kq < KG; ++kq) M = fmaxf(M, mls[((tct * KG + kq) * 8 + cl) * 2]);
+        float acc = 0.f, L = 0.f;
+#pragma unroll
+        for (int kq = 0; kq < KG; ++kq) {
+          const float mw = mls[((tct * KG + kq) * 8 + cl) * 2];
+          const float fw = (M == -INFINITY || mw == -INFINITY) ? 0.f : ex2(mw - M);
+          L += fw * mls[((tct * KG + kq) * 8 + cl) * 2 + 1];
+          acc += fw * om[((tct * KG + kq) * 8 + cl) * kMergeRow + sl];
+        }
+        if (!write) continue;
+        if (whole) {
+          const int qi = col_div(col, p.r), hh = col - qi * p.r;
+          const size_t orow = (size_t)(s * Q + qi) * H + g * p.r + hh;
+          static_cast<__nv_bfloat16*>(p.out)[orow * 128 + d] = __float2bfloat16_rn(L > 0.f ? __fdividef(acc, L) : 0.f);
+          if (d == 0 && p.lse) p.lse[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+        } else {
+          po[col * 128 + d] = acc;
+          if (d == 0) {
+            pml[2 * col] = M;
+            pml[2 * col + 1] = L;
+          }
+        }
       }
     }
+    // ---------------- the split that finishes its (sequence, group) last merges all
+    // of them.  The count is taken one item late: its atomic's answer is used
+    // only after the next item, so nothing waits on it.
+    named_bar_sync(1, kConsumers);  // every partial of this item written; the merge area is free again
+    if (pend_sg >= 0) {
+      if (tid == 0) *last_flag = (pend_old == pend_np - 1) ? 1 : 0;
+      named_bar_sync(1, kConsumers);
+      if (*last_flag) {
+        __threadfence();
+        merge_splits(p, pend_sg, pend_np, tid, true);
+      }
+      pend_sg = -1;
+    }
+    if (!whole && write) {
+      pend_sg = sg;
+      pend_np = (count + p.bps - 1) / p.bps;
+      if (tid == 0) pend_old = atomic_add_acq_rel(p.sg_ctr + sg, 1);  // releases the CTA's partials
+    }
+    if (dry) {
+      pdl_wait();  // the selection / union and the query fragments come from the preceding kernel
+    } else if (lane == 0) {
+      mbar_arrive(&iempty[slot]);
+    }
   }
-  const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  const size_t orow = (size_t)sq * H + h;
-  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + orow * 128 + 4 * lane;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t*>(&lo);
-  pk.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(outp) = pk;
-  if (lane == 0 && p.lse) p.lse[orow] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  if (pend_sg >= 0) {  // the last item's count
+    if (tid == 0) *last_flag = (pend_old == pend_np - 1) ? 1 : 0;
+    named_bar_sync(1, kConsumers);
+    if (*last_flag) {
+      __threadfence();
+      merge_splits(p, pend_sg, pend_np, tid, true);
+    }
+  }
+}
+
+// 168 registers a thread: ten warps of two CTAs spread 3/3/2/2 over the four
+// SM sub-partitions, 3 x 168 x 32 <= 16384 registers each.
+template <int FMT, int NT, int SP>
+__global__ void __maxnreg__(168)
+    attend_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const AttendParams p) {
+  using LY = AttLayout<FMT, NT, SP>;
+  constexpr int NST = LY::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + LY::BARS);
+  uint64_t* empty = full + NST;
+  uint64_t* ifull = empty + NST;
+  uint64_t* iempty = ifull + 2;
+  int* dead = reinterpret_cast<int*>(iempty + 2);
+  ItemFacts* facts = reinterpret_cast<ItemFacts*>(base + LY::FACTS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kWarps);
+    }
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(&ifull[sl], 1);
+      mbar_init(&iempty[sl], kWarps);
+    }
+    *dead = 0;
+    fence_mbar_init();
+    if constexpr (FMT != FMT_NVFP4) {
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmv);
+    }
+  }
+  __syncthreads();
+  // each role waits for the preceding kernel itself, after the work that does not need it
+  if (warp == kWarps) attend_producer<FMT, NT, SP>(&tmk, &tmv, p, base, full, empty, ifull, iempty, dead, facts, lane);
+  else attend_consumer<FMT, NT, SP>(p, base, full, empty, ifull, iempty, dead, facts, warp, lane);
 }
 
 cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, cudaLaunchAttribute* attr) {
@@ -751,64 +983,64 @@ cudaLaunchConfig_t pdl_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, 
 }
 
 template <int FMT, int NT, int SP>
-cudaError_t launch_att(const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, cudaStream_t st, bool pdl) {
+cudaError_t launch_att(const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, int num_sms,
+                       cudaStream_t st, bool pdl) {
   const size_t smem = AttLayout<FMT, NT, SP>::SMEM;
   auto kern = attend_kernel<FMT, NT, SP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  static int per_sm = 0;  // CTAs per SM for this instance (same on every device of one kind)
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
+  const long items = (long)p.batch.S * p.G * p.splits;
+  long grid = (long)per_sm * (num_sms > 0 ? num_sms : 1);
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_cfg(dim3((unsigned)(p.batch.S * p.G * p.splits)), dim3(kThreads), smem, st, pdl, attr);
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3((unsigned)grid), dim3(kThreads), smem, st, pdl, attr);
   CUtensorMap dummy = {};
   return cudaLaunchKernelEx(&cfg, kern, tk ? *tk : dummy, tv ? *tv : dummy, p);
 }
 
 template <int FMT>
-cudaError_t launch_att_fmt(const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, cudaStream_t st,
-                           bool pdl) {
+cudaError_t launch_att_fmt(const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, int num_sms,
+                           cudaStream_t st, bool pdl) {
   const int nt = p.geom.nt;
   if (p.geom.sp == 2) {
     if constexpr (FMT == FMT_FP8) {
       switch (nt) {
-        case 1: return launch_att<FMT, 1, 2>(tk, tv, p, st, pdl);
-        case 2: return launch_att<FMT, 2, 2>(tk, tv, p, st, pdl);
-        case 4: return launch_att<FMT, 4, 2>(tk, tv, p, st, pdl);
+        case 1: return launch_att<FMT, 1, 2>(tk, tv, p, num_sms, st, pdl);
+        case 2: return launch_att<FMT, 2, 2>(tk, tv, p, num_sms, st, pdl);
+        case 4: return launch_att<FMT, 4, 2>(tk, tv, p, num_sms, st, pdl);
         default: return cudaErrorInvalidValue;
       }
     }
     return cudaErrorInvalidValue;
   }
   switch (nt) {
-    case 1: return launch_att<FMT, 1, 1>(tk, tv, p, st, pdl);
-    case 2: return launch_att<FMT, 2, 1>(tk, tv, p, st, pdl);
-    case 4: return launch_att<FMT, 4, 1>(tk, tv, p, st, pdl);
+    case 1: return launch_att<FMT, 1, 1>(tk, tv, p, num_sms, st, pdl);
+    case 2: return launch_att<FMT, 2, 1>(tk, tv, p, num_sms, st, pdl);
+    case 4: return launch_att<FMT, 4, 1>(tk, tv, p, num_sms, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-int attend_stages(int fmt, int nt) {
-  if (fmt == FMT_FP8) return att_stages<FMT_FP8, 1>();
-  if (fmt == FMT_BF16) return att_stages<FMT_BF16, 1>();
-  return nt == 1 ? att_stages<FMT_NVFP4, 1>() : att_stages<FMT_NVFP4, 2>();
-}
-
 cudaError_t launch_attend(int fmt, const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, int num_sms,
                           cudaStream_t st, bool pdl) {
-  (void)num_sms;
   switch (fmt) {
-    case FMT_FP8: return launch_att_fmt<FMT_FP8>(tk, tv, p, st, pdl);
-    case FMT_BF16: return launch_att_fmt<FMT_BF16>(tk, tv, p, st, pdl);
-    case FMT_NVFP4: return launch_att_fmt<FMT_NVFP4>(tk, tv, p, st, pdl);
+    case FMT_FP8: return launch_att_fmt<FMT_FP8>(tk, tv, p, num_sms, st, pdl);
+    case FMT_BF16: return launch_att_fmt<FMT_BF16>(tk, tv, p, num_sms, st, pdl);
+    case FMT_NVFP4: return launch_att_fmt<FMT_NVFP4>(tk, tv, p, num_sms, st, pdl);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
-  const int rows = p.S * p.Q * p.G * p.r;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_cfg(dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, st, pdl, attr);
-  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 }  // namespace msa

@@ -54,6 +54,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// Plain arrival (no transaction bytes): completes a phase whose only
+// expected arrival is this one.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Wait until the phase with the given parity completes.  Bounded: each
 // try_wait returns after a short, implementation-defined time if the phase is
 // still open; after ~max_tries of them (a few seconds at most) it gives up and
@@ -112,6 +118,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- named barriers (ids > 0)
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over nthreads threads that also returns the OR of their predicates.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, %2, %3, q; selp.u32 %0, 1, 0, p; }"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------- PDL
@@ -205,14 +228,16 @@ __device__ __forceinline__ void split_e4m3(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
-// Largest e with amax * 2^e <= lim (amax > 0); 0 for amax == 0.
+// Largest e with amax * 2^e <= lim (amax > 0 and finite); 0 for zero, NaN or
+// infinite amax.  The corrections after the frexp estimate are bounded, so
+// any input ends.
 __device__ __forceinline__ int pow2_fit(float amax, float lim) {
-  if (!(amax > 0.f)) return 0;
+  if (!(amax > 0.f) || !(amax <= 3.0e38f)) return 0;
   int e;
   frexpf(lim / amax, &e);  // lim/amax = f * 2^e, f in [0.5, 1)
   e -= 1;
-  while (ldexpf(amax, e) > lim) --e;
-  while (ldexpf(amax, e + 1) <= lim) ++e;
+  for (int t = 0; t < 4 && ldexpf(amax, e) > lim; ++t) --e;
+  for (int t = 0; t < 4 && ldexpf(amax, e + 1) <= lim; ++t) ++e;
   return e;
 }
 

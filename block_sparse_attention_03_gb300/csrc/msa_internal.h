@@ -132,8 +132,8 @@ struct AttendParams {
   int32_t splits;
   const uint32_t* frag;     // [S*G][geom.words_per_unit()] query fragments (preceding kernel)
   const float* colf;        // [S*G][geom.nt*8] column factors
-  int32_t* work_ctr;        // unit counter (zeroed by the preceding kernel)
-  int32_t* sg_ctr;          // [S*G] partials written per (sequence, group) (zeroed likewise)
+  int32_t* work_ctr;        // unused
+  int32_t* sg_ctr;          // [S*G] splits finished per (sequence, group), zeroed by the preceding kernel
   float* part_o;            // [S*G][splits][cols][128]
   float* part_ml;           // [S*G][splits][cols][2]
   void* out;                // bf16 [S*Q][G*r][128]
@@ -141,15 +141,6 @@ struct AttendParams {
   DeviceStatus* status;
 };
 
-struct CombineParams {
-  int32_t S, Q, G, r, splits, cols, bps, topk, direct;
-  const int32_t* topk_idx;  // direct mode: [S][G][topk]
-  const int32_t* u_count;   // union mode: [S][G]
-  const float* part_o;
-  const float* part_ml;
-  void* out;   // bf16 [S*Q][G*r][128]
-  float* lse;  // [S*Q][G*r] or null
-};
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
@@ -158,8 +149,18 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attend(int fmt, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, const AttendParams& p,
                           int num_sms, cudaStream_t st, bool pdl);
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
-int attend_stages(int fmt, int nt);  // blocks one attend CTA holds in flight (= blocks per split)
+// Blocks per split of the attend: the (sequence, group) units are cut into
+// about as many splits as there are CTA slots on the GPU (slots / units
+// splits each), so every CTA gets about one split; 2 to 16 blocks a split
+// (a split of one block costs more in its partial and merge than it saves).
+constexpr int kMaxBlocksPerSplit = 16;
+inline int attend_blocks_per_split(int cap_blocks, long units, int cta_slots) {
+  long want = units > 0 ? cta_slots / units : 1;
+  if (want < 1) want = 1;
+  int bps = (int)((cap_blocks + want - 1) / want);
+  if (bps < 2) bps = 2;
+  return bps > kMaxBlocksPerSplit ? kMaxBlocksPerSplit : bps;
+}
 cudaError_t launch_dequant(int fmt, int which, const msa_cache_t& c, const int32_t* phys, int32_t n, float* out,
                            cudaStream_t st);
 

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
   __shared__ uint32_t ck[kCandMax];
   __shared__ uint8_t csel[kCandMax];
 
+  // the attend that follows may start its prologue now; it waits for this grid to finish
+  pdl_launch_dependents();
   const BatchDev bt = p.batch;
   const int row = blockIdx.x;  // (s*Q + i) * G + g
   const bool real_row = row < bt.S * bt.Q * p.G;
@@ -350,6 +352,7 @@ __global__ void __launch_bounds__(256) union_kernel(const UnionParams p) {
   int* ids = sh;                                      // [cap]
   int* first = sh + p.cap;                            // [cap] 1 if first occurrence
   uint32_t* masks = reinterpret_cast<uint32_t*>(sh + 2 * p.cap);  // [cap]
+  pdl_launch_dependents();  // the attend that follows may start its prologue; it waits for this grid
   pdl_wait();
   if (p.zero) {  // clear the attend's work counters for this call
     for (int z = blockIdx.x * blockDim.x + threadIdx.x; z < p.nzero; z += gridDim.x * blockDim.x) p.zero[z] = 0;

@@ -68,14 +68,15 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
-    # 4 long sequences with 8 new tokens each: the per-split partials alone exceed the scratch
-    w = ms.make_workload("fp8_decode", seq_lens=(60000,) * 4, q_per_seq=8, seed=93)
+    # 256 sequences with 8 new tokens each: one partial per (sequence, group) of
+    # 32 query x head columns is already 16 MiB, twice the scratch
+    w = ms.make_workload("fp8_decode", seq_lens=(2048,) * 256, q_per_seq=8, seed=93)
     case = ms.make_case(w, device="cuda")
     cache, batch, iq, q = bind(case)
     cfg = msa.default_config()
     assert msa.msa_workspace_size(cache, batch, cfg, 16) > 8 << 20
-    topk = torch.empty((4 * 8, 4, 16), dtype=torch.int32, device="cuda")
-    out = torch.empty((4 * 8, 16, 128), dtype=torch.bfloat16, device="cuda")
+    topk = torch.empty((256 * 8, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((256 * 8, 16, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(msa.MsaError) as e:
         msa.msa_decode_noalloc(cache, batch, cfg, iq, q, 16, topk, out, None)
     assert e.value.status == 3
