@@ -40,6 +40,28 @@ def kernels_per_step(q_per_seq: int) -> int:
     return 3 if q_per_seq == 1 else 4
 
 
+def ncu_traffic(workload: str):
+    """DRAM bytes (read + write) of one indexer launch from the committed ncu
+    summary of this workload, or None when there is none."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", f"indexer_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    total = 0.0
+    for name in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+        for line in text.splitlines():
+            cells = [c.strip() for c in line.split("|")]
+            if len(cells) > 2 and cells[1] == name:
+                val, _, unit = cells[2].partition(" ")
+                total += float(val) * scale.get(unit.strip(), 1.0)
+                break
+        else:
+            return None
+    return total
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,7 +417,8 @@ def main():
             "bytes_per_step": {"algorithmic": step_bytes, "index": idx_bytes, "kv_selected": kv_bytes,
                                "with_fp32_scales": actual_bytes},
             "roofline": ({"bound": "hbm", "kernel": "indexer_kernel (score + block max-pool)", "achieved": idx_gbs,
-                          "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                          "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
+                          "traffic": ncu_traffic(args.workload),
                           "peak_kind": peak_kind} if w.q_per_seq <= 8 else
                          {"bound": "tensor", "kernel": "indexer_kernel (score + block max-pool)",
                           "achieved": indexer_flops(w) / (idx_ms * 1e-3) / 1e12,
