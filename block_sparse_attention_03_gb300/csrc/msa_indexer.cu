@@ -194,24 +194,65 @@ __device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* 
   }
 }
 
-// Per-unit facts, packed as (code, seq_len): code >= 0 physical block,
-// -1 past the sequence's end, -2 bad data (flag raised), -3 past the last unit.
-__device__ __forceinline__ int2 unit_info(const IndexerParams& p, long u, long total) {
-  const BatchDev& bt = p.batch;
-  if (u >= total) return make_int2(-3, 0);
-  const int s = (int)(u % bt.S), b = (int)(u / bt.S);
+// Blocks of sequence s that hold keys (0 for a sequence length outside
+// [Q, max_blocks * 128], whose rows the kernel leaves at -inf).
+__device__ __forceinline__ int seq_blocks(const BatchDev& bt, int s) {
   const int T = bt.seq_len(s);
-  if (T < bt.Q || T > bt.max_nb * kBlock) {
-    if (b == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
-    return make_int2(-2, T);
+  return (T < bt.Q || T > bt.max_nb * kBlock) ? 0 : (T + kBlock - 1) / kBlock;
+}
+
+// (s, b) of the unit `adv` units after (s, b) in the sequence-major order of
+// all blocks that hold keys; s = S past the last one.
+__device__ __forceinline__ void advance_unit(const BatchDev& bt, int& s, int& b, long adv) {
+  long bb = b + adv;
+  while (s < bt.S) {
+    const int nb = seq_blocks(bt, s);
+    if (bb < nb) break;
+    bb -= nb;
+    ++s;
   }
-  if (b >= (T + kBlock - 1) / kBlock) return make_int2(-1, T);
+  b = (int)bb;
+}
+
+// (s, b) of unit v (v < total units), by the whole warp: 32 sequences a
+// step, an inclusive scan of their block counts finds the one holding v.
+__device__ __forceinline__ void locate_unit(const BatchDev& bt, long v, int lane, int& s_out, int& b_out) {
+  long base = 0;
+  s_out = bt.S;
+  b_out = 0;
+  for (int s0 = 0; s0 < bt.S; s0 += 32) {
+    const int sl = s0 + lane;
+    const int nb = (sl < bt.S) ? seq_blocks(bt, sl) : 0;
+    long inc = nb;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const long total = __shfl_sync(0xffffffffu, inc, 31);
+    if (v < base + total) {
+      const unsigned hit = __ballot_sync(0xffffffffu, v < base + inc);
+      const int l = __ffs(hit) - 1;
+      const long before = __shfl_sync(0xffffffffu, inc - nb, l);
+      s_out = s0 + l;
+      b_out = (int)(v - base - before);
+      return;
+    }
+    base += total;
+  }
+}
+
+// Facts of one unit: (code, seq_len, s, b); code >= 0 physical block, -2 bad
+// block-table entry (flag raised), -3 past the warp's last unit.
+__device__ __forceinline__ int4 unit_facts(const IndexerParams& p, int s, int b, bool live) {
+  const BatchDev& bt = p.batch;
+  if (!live || s >= bt.S) return make_int4(-3, 0, 0, 0);
+  const int T = bt.seq_len(s);
   const int phys = __ldg(bt.row(s) + b);
   if (phys < 0 || phys >= p.num_blocks) {
     raise_flag(p.status, FLAG_BAD_BLOCK, phys);
-    return make_int2(-2, T);
+    return make_int4(-2, T, s, b);
   }
-  return make_int2(phys, T);
+  return make_int4(phys, T, s, b);
 }
 
 template <int FMT, int NT, int SP>
@@ -229,9 +270,27 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
 
   const BatchDev bt = p.batch;
   const int S = bt.S, Q = bt.Q, G = p.G;
-  const long total = (long)S * bt.max_nb;
   const long gw = (long)blockIdx.x * WARPS + warp;
   const long tw = (long)gridDim.x * WARPS;
+
+  // Work: the blocks that hold keys, sequence-major, cut into one contiguous
+  // run per warp of equal length (+-1) -- balanced whatever the sequence
+  // lengths, and a warp's query fragments change only where its run crosses
+  // into the next sequence.  Each warp counts the units itself.
+  long V = 0;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int sl = s0 + lane;
+    int nb = 0;
+    if (sl < S) {
+      nb = seq_blocks(bt, sl);
+      if (nb == 0 && gw == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, sl);
+    }
+    for (int o = 16; o > 0; o >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    V += nb;
+  }
+  const long v0 = gw * V / tw, v1 = (gw + 1) * V / tw;  // this warp's units [v0, v1)
+  int ws, wb;  // (s, b) of unit v0 + it0 (the fact window's first unit)
+  locate_unit(bt, v0, lane, ws, wb);
 
   if (lane == 0) {
     for (int st = 0; st < NST; ++st) mbar_init(&bars[st], 1);
@@ -240,17 +299,25 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
   }
   // unit facts for iterations [it0, it0 + 64): lane l holds it0 + l and it0 + 32 + l
   long it0 = 0;
-  int2 inf0 = unit_info(p, gw + (long)lane * tw, total);
-  int2 inf1 = unit_info(p, gw + (long)(32 + lane) * tw, total);
+  auto facts_at = [&](int s_, int b_, long first) -> int4 {
+    int fs = s_, fb = b_;
+    advance_unit(bt, fs, fb, lane);
+    return unit_facts(p, fs, fb, v0 + first + lane < v1);
+  };
+  int4 inf0 = facts_at(ws, wb, 0);
+  int ws1 = ws, wb1 = wb;
+  advance_unit(bt, ws1, wb1, 32);
+  int4 inf1 = facts_at(ws1, wb1, 32);
   __syncwarp();
 
-  auto info_at = [&](long it) -> int2 {
+  auto info_at = [&](long it) -> int4 {
     const int idx = (int)(it - it0);
-    const int2 v = (idx < 32) ? inf0 : inf1;
-    return make_int2(__shfl_sync(0xffffffffu, v.x, idx & 31), __shfl_sync(0xffffffffu, v.y, idx & 31));
+    const int4 v = (idx < 32) ? inf0 : inf1;
+    return make_int4(__shfl_sync(0xffffffffu, v.x, idx & 31), __shfl_sync(0xffffffffu, v.y, idx & 31),
+                     __shfl_sync(0xffffffffu, v.z, idx & 31), __shfl_sync(0xffffffffu, v.w, idx & 31));
   };
   // copy the block of iteration `it` (facts `inf`) into stage st; lane 0 issues
-  auto issue = [&](long it, int2 inf, int st) {
+  auto issue = [&](long it, int4 inf, int st) {
     if (lane == 0 && inf.x >= 0) {
       const int phys = inf.x;
       uint8_t* dst = tiles + (size_t)st * TR::TILE;
@@ -284,13 +351,16 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
     if (it - it0 == 32) {  // slide the window of unit facts
       inf0 = inf1;
       it0 += 32;
-      inf1 = unit_info(p, gw + (it0 + 32 + lane) * tw, total);
+      ws = ws1;
+      wb = wb1;
+      advance_unit(bt, ws1, wb1, 32);
+      inf1 = facts_at(ws1, wb1, it0 + 32);
     }
-    const int2 inf = info_at(it);
+    const int4 inf = info_at(it);
     if (inf.x == -3) break;
-    const long u = gw + it * tw;
+    const long u = v0 + it;
     const int st = (int)(it % NST);
-    const int s = (int)(u % S), b = (int)(u / S);
+    const int s = inf.z, b = inf.w;
     float* prow = p.pooled + (size_t)s * Q * G * bt.max_nb + b;
     if (inf.x >= 0 && !dead) {
       if (s != cur_s) {
@@ -343,6 +413,17 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
     }
     __syncwarp();
     if (!dead) issue(it + NST, info_at(it + NST), st);
+  }
+  // blocks that hold no key of a sequence (past its length, or all of a bad
+  // sequence): -inf for every (query, group) row, spread over all threads
+  {
+    const long slots = (long)S * bt.max_nb;
+    for (long e = gw * 32 + lane; e < slots; e += tw * 32) {
+      const int s = (int)(e / bt.max_nb), b = (int)(e % bt.max_nb);
+      if (b < seq_blocks(bt, s)) continue;
+      float* prow = p.pooled + (size_t)s * Q * G * bt.max_nb + b;
+      for (int col = 0; col < Q * G; ++col) prow[(size_t)col * bt.max_nb] = -INFINITY;
+    }
   }
   pdl_launch_dependents();
   // a warp that gave up waits (bounded) for copies still in flight before exiting
