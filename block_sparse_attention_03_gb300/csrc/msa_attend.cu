@@ -156,6 +156,12 @@ __device__ __forceinline__ int fit448(float v) {
   return ((u & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;
 }
 
+// Phases of attend_block: 1 logits, 2 softmax, 4 P tile, 8 O^T += V^T P.
+// A real block runs all of them; the dry run before the grid-dependency wait
+// gives each consumer warp one phase, so the four warps fetch the four parts
+// of the instruction path at the same time instead of one after the other.
+constexpr unsigned kAllPhases = 15u;
+
 // One block of keys for one consumer warp.  The four consumer warps split the
 // work as NT column tiles x (4 / NT) key ranges: warp w takes column tile
 // ct = w / (4 / NT) (8 query x head columns) and the KW = 32 * NT keys
@@ -166,7 +172,7 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
                                              const uint32_t* __restrict__ fr, int ct, const float (&colf)[2],
                                              const int (&qlim)[2], const int (&qbit)[2], uint32_t qmask, int key0,
                                              int kw, int warp, int lane, float (&m_run)[2], float (&l_run)[2],
-                                             float (&o)[8][4], int& e_prev) {
+                                             float (&o)[8][4], int& e_prev, unsigned phases = kAllPhases) {
   using TR = AttTraits<FMT>;
   constexpr int MT = 2 * NT;  // m tiles of 16 keys
   constexpr int KW = 16 * MT; // keys of this warp
@@ -179,6 +185,7 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
   const uint32_t kt = smem_u32(stg);
+  if (phases & 1u) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
@@ -233,8 +240,11 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
       }
     }
   }
+  }
 
   // ---------------- scale, mask, online softmax (per column, over this warp's keys)
+  float alpha[2] = {0.f, 0.f};
+  if (phases & 2u) {
   float ksc[MT][2];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -245,7 +255,6 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
         v = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE)[kw + 16 * mt + g8 + 8 * hh];
       ksc[mt][hh] = v;
     }
-  float alpha[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const bool sel = (qmask >> qbit[c]) & 1u;
@@ -280,9 +289,11 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
     l_run[c] = l_run[c] * alpha[c] + psum;
     m_run[c] = mnew;
   }
+  }
 
   // ---------------- P operand into this warp's shared tile
   __syncwarp();
+  if (phases & 4u) {
   if constexpr (FMT == FMT_FP8) {
     // P' = p * vscale * 2^e, split into e4m3 hi + lo; tile [term][column][KW bytes]
     const float* vsc = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE + TR::KSC);
@@ -393,12 +404,16 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
                        "r"(out[4 * cc + 2]), "r"(out[4 * cc + 3]));
         }
       }
-      if constexpr (NT > 1) named_bar_sync(2, kConsumers);  // other warps' rows are read below
+      if constexpr (NT > 1) {
+        if (phases == kAllPhases) named_bar_sync(2, kConsumers);  // other warps' rows are read below
+      }
     }
+  }
   }
   __syncwarp();
 
   // ---------------- O^T += V^T P
+  if (phases & 8u) {
   if constexpr (FMT == FMT_FP8) {
     const uint32_t vt = smem_u32(stg + TR::KTILE);
     const int cg = (g8 >> 1) | ((g8 & 1) << 2);  // this lane's 16-dim chunk
@@ -462,7 +477,10 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
           mma_f16_k16(o[mm], a, bp0, bp1);
       }
     }
-    if constexpr (FMT == FMT_NVFP4 && NT > 1) named_bar_sync(2, kConsumers);  // before the tile is rewritten
+    if constexpr (FMT == FMT_NVFP4 && NT > 1) {
+      if (phases == kAllPhases) named_bar_sync(2, kConsumers);  // before the tile is rewritten
+    }
+  }
   }
   __syncwarp();
 }
@@ -482,6 +500,8 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const 
   return mbar_wait_warp(bar, parity);
 }
 
+__device__ __noinline__ void merge_splits(const AttendParams& p, int sg, int nparts, int tid, bool write);
+
 template <int FMT, int NT, int SP>
 __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttendParams& p,
                                                 uint8_t* base, uint64_t* full, uint64_t* empty, uint64_t* ifull,
@@ -492,32 +512,37 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
   constexpr int NST = LY::NST;
   const BatchDev bt = p.batch;
   const int G = p.G;
-  const long items = (long)bt.S * G * p.splits;
-  const long stride = gridDim.x;
-  long bi = 0;  // blocks pushed through the ring
-  long ii = 0;  // items published
+  const int items = bt.S * G * p.splits;  // 32-bit: no 64-bit divisions below
+  const int stride = gridDim.x;
+  int bi = 0;  // blocks pushed through the ring
+  int ii = 0;  // items published
   bool ok = true;
   bool waited = false;
-  for (long it0 = blockIdx.x; it0 < items && ok; it0 += 32 * stride) {
+#pragma unroll 1
+  for (int it0 = blockIdx.x; it0 < items && ok; it0 += 32 * stride) {
     // selected-block counts of the next 32 items of this CTA, one per lane.  One
     // query token: the top-k keeps min(k, visible blocks) blocks, known from the
     // sequence length alone (a caller input, readable before the wait).
-    const long my_it = it0 + lane * stride;
+    const int my_it = it0 + lane * stride;
     int my_cnt = 0;
     if (p.direct && my_it < items) {
-      const int T = bt.seq_len((int)(my_it / p.splits) / G);
+      const int T = bt.seq_len(my_it / p.splits / G);
       my_cnt = (T < 1 || T > bt.max_nb * kBlock) ? 0 : min(p.topk, (T - 1) / kBlock + 1);
     }
     if (!waited) {
+      // meanwhile the consumers fetch the block code; fetch the split merge's
+      // (a pass over the first split's partials of the previous call, nothing written)
+      merge_splits(p, 0, 1, lane, false);
       pdl_wait();  // the selection / union and the query fragments come from the preceding kernel
       waited = true;
     }
-    if (!p.direct && my_it < items) my_cnt = p.u_count[(int)(my_it / p.splits)];
+    if (!p.direct && my_it < items) my_cnt = p.u_count[my_it / p.splits];
+#pragma unroll 1
     for (int t = 0; t < 32 && ok; ++t) {
-      const long it = it0 + t * stride;
+      const int it = it0 + t * stride;
       if (it >= items) break;
       const int count = __shfl_sync(0xffffffffu, my_cnt, t);
-      const int sg = (int)(it / p.splits), split = (int)(it % p.splits);
+      const int sg = it / p.splits, split = it - sg * p.splits;
       const int kb0 = split * p.bps;
       const int n = max(0, min(p.bps, count - kb0));
       const bool empty_sg = count <= 0;
@@ -545,7 +570,7 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
       }
       // publish the item
       const int slot = (int)(ii & 1);
-      const long use = ii >> 1;
+      const int use = ii >> 1;
       if (use > 0 && !ring_wait(&iempty[slot], (uint32_t)((use - 1) & 1), dead)) {
         set_dead(dead, p.status, (int)it);
         ok = false;
@@ -578,10 +603,11 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
       }
       ++ii;
       // its blocks, through the ring
+#pragma unroll 1
       for (int k = 0; k < n; ++k) {
         const int ph = __shfl_sync(0xffffffffu, phys, k);
         const int st = (int)(bi % NST);
-        const long ub = bi / NST;
+        const int ub = bi / NST;
         if (ub > 0 && !ring_wait(&empty[st], (uint32_t)((ub - 1) & 1), dead)) {
           set_dead(dead, p.status, (int)it);
           ok = false;
@@ -621,7 +647,7 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
   // end of the stream
   if (ok) {
     const int slot = (int)(ii & 1);
-    const long use = ii >> 1;
+    const int use = ii >> 1;
     if (use > 0 && !ring_wait(&iempty[slot], (uint32_t)((use - 1) & 1), dead)) {
       set_dead(dead, p.status, -1);
     } else if (lane == 0) {
@@ -634,11 +660,11 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
   // (immediate in a healthy run: the consumers waited for all of them)
   if (lane == 0) {
     for (int st = 0; st < NST; ++st) {
-      const long uses = bi > st ? (bi - 1 - st) / NST + 1 : 0;
+      const int uses = bi > st ? (bi - 1 - st) / NST + 1 : 0;
       if (uses > 0) mbar_wait(&full[st], (uint32_t)((uses - 1) & 1), 2000);
     }
     for (int sl = 0; sl < 2; ++sl) {
-      const long uses = ii > sl ? (ii - 1 - sl) / 2 + 1 : 0;
+      const int uses = ii > sl ? (ii - 1 - sl) / 2 + 1 : 0;
       if (uses > 0) mbar_wait(&ifull[sl], (uint32_t)((uses - 1) & 1), 2000);
     }
   }
@@ -661,10 +687,12 @@ __device__ __noinline__ void merge_splits(const AttendParams& p, int sg, int npa
   const int G = p.G, Q = p.batch.Q, cols = p.geom.cols, H = G * p.r;
   const int s = sg / G, g = sg % G;
   const size_t pbase = (size_t)sg * p.splits;
+#pragma unroll 1
   for (int e = tid; e < cols * 32; e += kConsumers) {
     const int col = e >> 5, d4 = (e & 31) * 4;
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
     for (int i0 = 0; i0 < nparts; i0 += 8) {
       float mi[8], li[8];
       float4 oi[8];
@@ -733,12 +761,13 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
   float* om = reinterpret_cast<float*>(base + LY::MERGE);  // KG > 1: [4 warps][8 cols][kMergeRow]
   float* mls = om + (size_t)kWarps * 8 * kMergeRow;        // [4][8][2]: running max, row sum
   int* last_flag = reinterpret_cast<int*>(base + LY::MERGE + LY::MERGE_BYTES);
-  long bi = 0;
+  int bi = 0;
   int pend_sg = -1, pend_np = 0, pend_old = 0;  // the previous item's split count (answer in thread 0)
   // Item -1 is a dry run before the grid dependency wait: the same code over
   // the first stage with every key masked and no global writes, so that the
   // instruction path is fetched while the preceding kernel still runs.
-  for (long ii = -1;; ++ii) {
+#pragma unroll 1
+  for (int ii = -1;; ++ii) {
     const bool dry = ii < 0;
     const int slot = dry ? 0 : (int)(ii & 1);
     bool got = true;
@@ -773,6 +802,7 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
       for (int mm = 0; mm < 8; ++mm) o[mm][c] = o[mm][c + 2] = 0.f;
     }
 
+#pragma unroll 1
     for (int k = 0; k < n; ++k) {
       const int st = dry ? 0 : (int)(bi % NST);
       bool have = true;
@@ -788,7 +818,7 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
       if (have && (dry || f.sok[k])) {
         attend_block<FMT, NT, SP>(base + (size_t)st * LY::STAGE, psm, vdq, fr, ct, colf, qlim, qbit,
                                   dry ? 0u : f.smask[k], (dry ? 0 : f.sb[k]) * kBlock + kw, kw, warp, lane, m_run,
-                                  l_run, o, e_prev);
+                                  l_run, o, e_prev, dry ? (1u << warp) : kAllPhases);
       }
       __syncwarp();
       if (!dry && lane == 0) mbar_arrive(&empty[st]);
@@ -860,6 +890,7 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
             om[(warp * 8 + cl) * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
       }
       named_bar_sync(1, kConsumers);
+#pragma unroll 1
       for (int e = tid; e < NT * 8 * 128; e += kConsumers) {
         const int tct = e >> 10, cl = (e >> 7) & 7, sl = e & 127;  // tile, column, accumulator row
         const int col = tct * 8 + cl;

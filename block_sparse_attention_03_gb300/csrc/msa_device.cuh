@@ -66,6 +66,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 4000000) {
   const uint32_t a = smem_u32(bar);
+#pragma unroll 1
   for (int i = 0; i < max_tries; ++i) {
     uint32_t done;
     asm volatile(
@@ -81,6 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int ma
 // Warp-uniform wait: every lane polls, the warp agrees on the outcome.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int max_tries = 4000000) {
   const uint32_t a = smem_u32(bar);
+#pragma unroll 1
   for (int i = 0; i < max_tries; ++i) {
     uint32_t done;
     asm volatile(
