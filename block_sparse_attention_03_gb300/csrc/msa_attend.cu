@@ -529,6 +529,13 @@ __device__ __forceinline__ void attend_producer(const CUtensorMap* tmk, const CU
       const int T = bt.seq_len(my_it / p.splits / G);
       my_cnt = (T < 1 || T > bt.max_nb * kBlock) ? 0 : min(p.topk, (T - 1) / kBlock + 1);
     }
+    if (!waited && my_it < items) {
+      // the block-table row of this lane's item into L2 (caller input, readable now):
+      // the physical-block lookups after the wait then hit
+      const int32_t* rowp = bt.row(my_it / p.splits / G);
+      for (int e = 0; e < bt.max_nb && e < 64 * 32; e += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rowp + e));
+    }
     if (!waited) {
       // meanwhile the consumers fetch the block code; fetch the split merge's
       // (a pass over the first split's partials of the previous call, nothing written)

@@ -432,8 +432,8 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   const unsigned rows = (unsigned)(p.batch.S * p.batch.Q * p.G);
-  // long rows: 1024 threads (more warps to hide latency, 4x fewer keys each)
-  const bool wide = p.batch.max_nb > 1024;
+  // rows beyond what 256 threads hold in registers (16 keys each): 1024 threads
+  const bool wide = p.batch.max_nb > kTopkThreads * kKeysPerThreadNarrow;
   const unsigned threads = wide ? 1024u : (unsigned)kTopkThreads;
   const unsigned zrows = (unsigned)((p.nzero + threads - 1) / threads);
   cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(threads), 0, st, pdl, attr);

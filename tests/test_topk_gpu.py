@@ -87,10 +87,19 @@ def test_topk_short_rows(kind):
 
 @pytest.mark.parametrize("kind", ["normal", "ties", "ties2", "equal", "neg_inf"])
 def test_topk_long_rows(kind):
-    # more than 1024 blocks per row: the 1024-thread variant, keys in registers
+    # up to 4096 blocks per row: 256 threads x 16 keys in registers
     rng = np.random.default_rng(200 + len(kind))
     seq_lens = [128 * 1025 + 3, 524288, 300]
     mb = 4096
+    _check(seq_lens, 1, mb, _scores(rng, len(seq_lens), mb, kind), msa.Config(topk=16))
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties2"])
+def test_topk_wide_rows(kind):
+    # 4097 .. 8192 blocks per row: the 1024-thread variant, 8 keys each in registers
+    rng = np.random.default_rng(250 + len(kind))
+    seq_lens = [128 * 6000, 128 * 4097 + 1, 128 * 50]
+    mb = 6000
     _check(seq_lens, 1, mb, _scores(rng, len(seq_lens), mb, kind), msa.Config(topk=16))
 
 
