@@ -882,9 +882,13 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
         }
       }
     } else {
-      // the KG warps of a column tile hold different keys: merge them in shared memory
+      // the KG warps of a column tile hold different keys: merge them in shared
+      // memory.  In the dry run, half of the warps take the stores and half the
+      // merge loop, without barriers, so both parts are fetched at once.
+      const bool seg_store = !dry || (warp & 1) == 0;
+      const bool seg_merge = !dry || (warp & 1) == 1;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 2 && seg_store; ++c) {
         const int cl = 2 * j + c;
         if (g8 == 0) {
           mls[(warp * 8 + cl) * 2] = wdead ? -INFINITY : m_run[c];
@@ -896,9 +900,9 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
           for (int h2 = 0; h2 < 2; ++h2)
             om[(warp * 8 + cl) * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
       }
-      named_bar_sync(1, kConsumers);
+      if (!dry) named_bar_sync(1, kConsumers);
 #pragma unroll 1
-      for (int e = tid; e < NT * 8 * 128; e += kConsumers) {
+      for (int e = tid; e < NT * 8 * 128 && seg_merge; e += kConsumers) {
         const int tct = e >> 10, cl = (e >> 7) & 7, sl = e & 127;  // tile, column, accumulator row
         const int col = tct * 8 + cl;
         if (col >= cols) continue;
@@ -938,7 +942,7 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
     // ---------------- the split that finishes its (sequence, group) last merges all
     // of them.  The count is taken one item late: its atomic's answer is used
     // only after the next item, so nothing waits on it.
-    named_bar_sync(1, kConsumers);  // every partial of this item written; the merge area is free again
+    if (!dry) named_bar_sync(1, kConsumers);  // every partial of this item written; the merge area is free again
     if (pend_sg >= 0) {
       if (tid == 0) *last_flag = (pend_old == pend_np - 1) ? 1 : 0;
       named_bar_sync(1, kConsumers);
