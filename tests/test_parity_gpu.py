@@ -194,6 +194,25 @@ def test_full_size_sampled(name, seqs):
         check_out(g["out"][rows], o)
 
 
+def test_many_short_sequences():
+    # 2,600 sequences of 1..700 tokens: more (sequence, group) units than the attend
+    # has CTAs by far, so every CTA walks dozens of splits in several batches
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 700, size=2600)
+    w = ms.make_workload("fp8_decode", seq_lens=lens, seed=77)
+    c = ms.make_case(w, device="cuda")
+    g = gpu_path(c)
+    h = ms.case_to_host(c)
+    del c
+    for s in [0, 1, 2, 777, 1500, 2599] + [int(x) for x in rng.choice(2600, 6, replace=False)]:
+        pooled = O.pooled_scores(h, s, w.index_dim ** -0.5)
+        full = np.full((w.num_seqs, w.num_kv_heads, w.max_blocks), -np.inf)
+        full[s] = pooled[0]
+        check_selection(g["topk"], full, w.seq_lens, 1, w.topk, rows=[s])
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        check_out(g["out"][[s]], o)
+
+
 def test_full_size_prefill_sampled():
     # 8,192 new tokens on a 64K-token FP8 context: sampled query rows against the oracle
     w = ms.make_workload("fp8_prefill")
