@@ -140,7 +140,8 @@ FragGeom geom_for(int key_fmt, bool q_fp8, int cols) {
 }
 
 struct Plan {
-  int S = 0, Q = 0, chunks = 1;  // sequences / query tokens as the kernels see them (long chunks split)
+  int S = 0, Q = 0, chunks = 1;  // indexer: sequences / query tokens as it sees them (long chunks split)
+  int Sa = 0, Qa = 0, chunks_a = 1;  // the same for the attend
   FragGeom gi, ga;          // indexer / attend query geometry
   int bps = 0, splits = 0, cap = 0, r = 0;
   bool direct = false;      // one query token: the attend reads the selection rows directly
@@ -164,16 +165,24 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.chunks = b->q_per_seq / QV;
   pl.S = b->num_seqs * pl.chunks;
   pl.Q = QV;
-  const int S = pl.S, Q = pl.Q, G = c->num_kv_heads;
+  // The attend of a prefill chunk runs every token as its own one-token
+  // sequence: neighbouring tokens' selections overlap little, so a union over
+  // 8 tokens would stream each block for 32 columns of which about 4 chose it.
+  // Up to 8 new tokens (speculative verify) share a union.
+  pl.Qa = b->q_per_seq > 8 ? 1 : QV;
+  pl.chunks_a = b->q_per_seq / pl.Qa;
+  pl.Sa = b->num_seqs * pl.chunks_a;
+  const int Q = pl.Q, G = c->num_kv_heads;
+  const int S = pl.Sa, Qa = pl.Qa;  // the attend's units size the buffers below
   if (hq < G || hq % G != 0) return MSA_ERR_INVALID_ARGUMENT;
   pl.r = hq / G;
   const int fi = fmt_of(c->index_dtype), fa = fmt_of(c->kv_dtype);
   pl.gi = geom_for(fi < 0 ? FMT_FP8 : fi, iq_fp8, Q * G);
-  pl.ga = geom_for(fa < 0 ? FMT_FP8 : fa, q_fp8, Q * pl.r);
+  pl.ga = geom_for(fa < 0 ? FMT_FP8 : fa, q_fp8, Qa * pl.r);
   if (pl.gi.nt > kMaxIndexerNT || pl.gi.nt * pl.gi.sp > 8) return MSA_ERR_UNSUPPORTED;
   if (pl.ga.cols > kMaxAttendCols || pl.ga.nt * pl.ga.sp > 8) return MSA_ERR_UNSUPPORTED;
-  pl.cap = Q * cfg->topk;
-  pl.direct = (b->q_per_seq == 1);
+  pl.cap = Qa * cfg->topk;
+  pl.direct = (Qa == 1);
   // a union never holds more blocks than a sequence has
   const int cap_eff = pl.cap < b->max_blocks_per_seq ? pl.cap : b->max_blocks_per_seq;
   pl.bps = attend_blocks_per_split(cap_eff, (long)S * G, 2 * sm_count());
@@ -181,7 +190,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.nctr = S * G;  // splits finished per (sequence, group)
   size_t o = 0;
   pl.off_status = o; o = align256(o + 256);
-  pl.off_pooled = o; o = align256(o + (size_t)S * Q * G * b->max_blocks_per_seq * 4);
+  pl.off_pooled = o; o = align256(o + (size_t)b->num_seqs * b->q_per_seq * G * b->max_blocks_per_seq * 4);
   pl.off_uids = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_umask = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_ucount = o; o = align256(o + (size_t)S * G * 4);
@@ -208,6 +217,15 @@ BatchDev batch_dev(const msa_batch_t* b, const Plan& pl) {
   d.max_nb = b->max_blocks_per_seq;
   d.chunks = pl.chunks;
   d.q_real = b->q_per_seq;
+  return d;
+}
+
+// the attend's view of the batch (its own virtual sequences)
+BatchDev batch_dev_att(const msa_batch_t* b, const Plan& pl) {
+  BatchDev d = batch_dev(b, pl);
+  d.S = pl.Sa;
+  d.Q = pl.Qa;
+  d.chunks = pl.chunks_a;
   return d;
 }
 
@@ -303,7 +321,7 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   DeviceStatus* status = at<DeviceStatus>(ws, pl.off_status);
   const bool direct = prepared && pl.direct;
   UnionParams up;
-  up.batch = batch_dev(b, pl);
+  up.batch = batch_dev_att(b, pl);
   up.G = G;
   up.topk = cfg->topk;
   up.topk_idx = topk_idx;
@@ -329,7 +347,7 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
     tvp = &tv;
   }
   AttendParams ap;
-  ap.batch = batch_dev(b, pl);
+  ap.batch = batch_dev_att(b, pl);
   ap.G = G;
   ap.r = pl.r;
   ap.num_blocks = c->num_blocks;
