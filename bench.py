@@ -40,10 +40,11 @@ def kernels_per_step(q_per_seq: int) -> int:
     return 3 if q_per_seq == 1 else 4
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes (read + write) of one indexer launch from the committed ncu
-    summary of this workload, or None when there is none."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", f"indexer_{workload}.md")
+def ncu_traffic(workload: str, kernel: str = "indexer"):
+    """DRAM bytes (read + write) of one launch of the kernel from the committed
+    ncu summary of this workload (profiles/<kernel>_<workload>.md), or None
+    when there is none."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -443,11 +444,11 @@ def main():
                           "peak": peak, "unit": "GB/s", "frac": idx_gbs / peak,
                           "traffic": ncu_traffic(args.workload),
                           "peak_kind": peak_kind} if w.q_per_seq <= 8 else
-                         {"bound": "tensor", "kernel": "indexer_kernel (score + block max-pool)",
+                         {"bound": "tensor", "kernel": "pindexer_kernel (tcgen05 score + block max-pool)",
                           "achieved": indexer_flops(w) / (idx_ms * 1e-3) / 1e12,
                           "peak": 2.0 * bf16_tflops, "unit": "TFLOP/s",
                           "frac": indexer_flops(w) / (idx_ms * 1e-3) / 1e12 / (2.0 * bf16_tflops),
-                          "traffic": None,
+                          "traffic": ncu_traffic(args.workload, "pindexer"),
                           "peak_kind": peak_kind + " (bf16 burst x 2 for e4m3, the nominal ratio)"}),
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -152,6 +152,13 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// A prefill chunk (more than 8 new tokens a sequence) over an FP8 index
+// cache: the tcgen05 indexer, with the query tokens as the MMA's M side.
+bool tc_indexer(const msa_cache_t* c, const msa_batch_t* b) {
+  const int G = c->num_kv_heads;
+  return fmt_of(c->index_dtype) == FMT_FP8 && b->q_per_seq > 8 && (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
 // Plan for the given problem.  iq_fp8 / q_fp8: query dtypes (E4M3 or bf16).
 msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, int hq, bool iq_fp8,
                        bool q_fp8, Plan& pl) {
@@ -179,7 +186,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   const int fi = fmt_of(c->index_dtype), fa = fmt_of(c->kv_dtype);
   pl.gi = geom_for(fi < 0 ? FMT_FP8 : fi, iq_fp8, Q * G);
   pl.ga = geom_for(fa < 0 ? FMT_FP8 : fa, q_fp8, Qa * pl.r);
-  if (pl.gi.nt > kMaxIndexerNT || pl.gi.nt * pl.gi.sp > 8) return MSA_ERR_UNSUPPORTED;
+  if (!tc_indexer(c, b) && (pl.gi.nt > kMaxIndexerNT || pl.gi.nt * pl.gi.sp > 8)) return MSA_ERR_UNSUPPORTED;
   if (pl.ga.cols > kMaxAttendCols || pl.ga.nt * pl.ga.sp > 8) return MSA_ERR_UNSUPPORTED;
   pl.cap = Qa * cfg->topk;
   pl.direct = (Qa == 1);
@@ -242,6 +249,25 @@ msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_c
   if (fi != FMT_NVFP4) {
     if (!encode_rows(&tm, c->idx, (long)c->num_blocks * kBlock, fi == FMT_BF16)) return MSA_ERR_CUDA;
     tmp = &tm;
+  }
+  if (tc_indexer(c, b)) {
+    // a prefill chunk: the queries fill the tensor cores' M side (tcgen05)
+    PrefillIndexerParams pp;
+    Plan real;
+    real.S = b->num_seqs;
+    real.Q = b->q_per_seq;
+    real.chunks = 1;
+    pp.batch = batch_dev(b, real);
+    pp.G = G;
+    pp.num_blocks = c->num_blocks;
+    pp.idx_scale = c->idx_scale;
+    pp.index_q = iq->data;
+    pp.iq_fp8 = iq->dtype == MSA_DTYPE_FP8_E4M3;
+    pp.iq_scale = pp.iq_fp8 ? iq->scale : 1.f;
+    pp.col_const = cfg->index_scale;
+    pp.pooled = pooled;
+    pp.status = at<DeviceStatus>(ws, pl.off_status);
+    return cuda_status(launch_prefill_indexer(tmp, pp, sm_count(), st));
   }
   IndexerParams ip;
   ip.batch = batch_dev(b, pl);

@@ -142,7 +142,24 @@ struct AttendParams {
 };
 
 
+// Prefill indexer on tcgen05 (FP8 index cache with per-token scales): the
+// real batch (no virtual sequences), pooled [S*Q][G][max_nb].
+struct PrefillIndexerParams {
+  BatchDev batch;
+  int32_t G;               // 1, 2, 4 or 8: 128 / G query tokens per 128-row tile
+  int32_t num_blocks;
+  const float* idx_scale;  // per-token fp32 scales of the index keys
+  const void* index_q;     // [S*Q][G][128] bf16 or e4m3 codes
+  int32_t iq_fp8;
+  float iq_scale;
+  float col_const;         // index_scale
+  float* pooled;
+  DeviceStatus* status;
+};
+
 // launchers (return cudaGetLastError())
+cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexerParams& p, int num_sms,
+                                   cudaStream_t st);
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
                            bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);

@@ -1,0 +1,526 @@
+// Indexer score + block max-pool for prefill chunks on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// What it computes is the indexer of the decode path (MiniMax Sparse Attention
+// model page, "Lightning indexer" / "Top-k block selection"; vLLM Day-0 blog,
+// the MSA indexer prefill kernel): for query token i of sequence s and group g,
+//   P[s, i, g, b] = col_const * max over keys t of block b with t <= pos(i) of
+//                   (index_q[s, i, g] . ik[t]) * kscale[t],
+// -inf where block b holds no visible key.  With thousands of new tokens the
+// contraction is dense, so the queries become the MMA's M side:
+//   D[128 x 128] = A[128 rows = (token, group)] x B[128 keys of one block]^T
+// with K = 128 index dims in four k32 steps of kind::f8f6f4 (e4m3 x e4m3).  A
+// bf16 index query is scaled by a power of two per row (exact) and split into
+// e4m3 hi + lo terms that accumulate into the same TMEM columns, carrying all 8
+// significant bits of bf16; an e4m3 index query enters as is.
+//
+// One CTA (10 warps, persistent, one per SM) walks a contiguous run of
+// (query tile, key block) pairs:
+//   warp 0   copies key tiles (TMA, 128-byte swizzle) into a 10-stage ring
+//            (enough bytes in flight to cover L2 latency at the MMA rate), freed
+//            by the MMAs' completion, and their per-token scales into a 16-slot
+//            ring freed by the epilogue;
+//   warp 1   owns the SM's 512 TMEM columns (four 128-column accumulators); one
+//            thread issues the MMAs and commits them to mbarriers;
+//   warps 2-9 two groups of four, taking alternate pairs; each thread owns one
+//            accumulator row (tcgen05.ld 32x32b), multiplies by the key scales
+//            (packed f32x2), masks the keys its token cannot see, takes the max
+//            (three-input max) and writes P.  At each new query tile both
+//            groups build its operand (hi / lo e4m3 in the swizzled K-major
+//            layout the MMA reads), group 0 the hi term, group 1 the lo term.
+// Every mbarrier wait is bounded; a wait that gives up sets the timeout flag,
+// the CTA stops issuing, drains what it issued and frees its TMEM.
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kPiStages = 10;                  // key tiles in flight: L2 latency x the MMA rate
+constexpr int kPiSStages = 16;                 // key-scale slots (released by the epilogue, which lags)
+constexpr int kPiAcc = 4;                      // accumulators of 128 columns
+constexpr int kPiCols = 128 * kPiAcc;          // TMEM columns (all 512 of the SM: one CTA per SM)
+constexpr int kPiThreads = 320;                // producer, MMA, 2 x 4 epilogue warps
+constexpr uint32_t kPiTile = 128 * 128;        // bytes of one e4m3 128 x 128 tile
+constexpr uint32_t kPiScales = 128 * 4;        // fp32 key scales of one block
+
+struct PiLayout {
+  static constexpr uint32_t A = 0;                                  // [2 terms][16 KB]
+  static constexpr uint32_t KT = 2 * kPiTile;                       // [stages][16 KB]
+  static constexpr uint32_t KS = KT + kPiStages * kPiTile;          // [scale slots][512 B]
+  static constexpr uint32_t BARS = KS + kPiSStages * kPiScales;     // mbarriers
+  // kfull, kempty, sfull, sempty, tfull, tempty, afull, aempty, done
+  static constexpr uint32_t NBARS = 2 * kPiStages + 2 * kPiSStages + 2 * kPiAcc + 3;
+  static constexpr uint32_t TSLOT = BARS + NBARS * 8;               // TMEM base from the allocator
+  static constexpr uint32_t DEAD = TSLOT + 4;
+  static constexpr uint32_t TOTAL = DEAD + 12;
+  static constexpr uint32_t SMEM = TOTAL + 1024;                    // 1024-byte alignment slack
+};
+
+// ---------------------------------------------------------------- tcgen05 wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (TMEM) = / += A (smem) x B (smem)^T, e4m3 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier when every MMA this thread issued so far is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// (a.x * b.x, a.y * b.y), round to nearest, one packed instruction
+__device__ __forceinline__ float2 mul2(float ax, float ay, float bx, float by) {
+  float2 r;
+  asm("{ .reg .b64 x, y, z; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %5}; mul.rn.f32x2 z, x, y; mov.b64 {%0, %1}, z; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by));
+  return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory operand descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the layout a 128-byte-swizzled TMA box of 128-byte rows
+// produces).  Start address in 16-byte units; the leading offset is unused
+// for this layout (1); descriptor version 1; swizzle code 2 = 128 B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: D fp32, A and B e4m3, both K-major, N = 128, M = 128.
+constexpr uint32_t kIdescF8 = (1u << 4) | (0u << 7) | (0u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+// ---------------------------------------------------------------- work walk
+
+// The pairs (sequence, query tile, key block) in order: sequence-major, then
+// tile, then block.  A sequence contributes tiles x (blocks that hold keys);
+// a malformed one (length outside [Q, max_blocks * 128]) none.
+struct PairCursor {
+  int s, qt, b;
+  int nb;  // blocks of sequence s (kept so that walking reads no memory)
+};
+
+__device__ __forceinline__ int pi_seq_blocks(const BatchDev& bt, int s) {
+  const int T = bt.seq_len(s);
+  if (T < bt.Q || T > bt.max_nb * kBlock) return 0;
+  return (T + kBlock - 1) / kBlock;
+}
+
+__device__ __forceinline__ void pi_locate(const BatchDev& bt, int tiles, long p, PairCursor& c) {
+  c.s = bt.S;
+  c.qt = c.b = c.nb = 0;
+  for (int s = 0; s < bt.S; ++s) {
+    const int nb = pi_seq_blocks(bt, s);
+    const long n = (long)tiles * nb;
+    if (p < n) {
+      c.s = s;
+      c.nb = nb;
+      c.qt = (int)(p / nb);
+      c.b = (int)(p % nb);
+      return;
+    }
+    p -= n;
+  }
+}
+
+// k pairs further on (past the last pair: s = S)
+__device__ __forceinline__ void pi_skip(const BatchDev& bt, int tiles, PairCursor& c, int k) {
+  c.b += k;
+  while (c.s < bt.S && c.b >= c.nb) {
+    c.b -= c.nb;
+    if (++c.qt < tiles) continue;
+    c.qt = 0;
+    c.nb = 0;
+    while (++c.s < bt.S) {
+      c.nb = pi_seq_blocks(bt, c.s);
+      if (c.nb > 0) break;
+    }
+  }
+}
+
+__device__ __forceinline__ void pi_advance(const BatchDev& bt, int tiles, PairCursor& c) { pi_skip(bt, tiles, c, 1); }
+
+__device__ __forceinline__ bool pi_wait(uint64_t* bar, uint32_t parity, int* dead, DeviceStatus* st, int where) {
+  if (*reinterpret_cast<volatile int*>(dead)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *reinterpret_cast<volatile int*>(dead) = 1;
+  raise_flag(st, FLAG_TIMEOUT, where);
+  return false;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+__global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                               const PrefillIndexerParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using LY = PiLayout;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(base + LY::BARS);
+  uint64_t* kempty = kfull + kPiStages;
+  uint64_t* sfull = kempty + kPiStages;
+  uint64_t* sempty = sfull + kPiSStages;
+  uint64_t* tfull = sempty + kPiSStages;
+  uint64_t* tempty = tfull + kPiAcc;
+  uint64_t* afull = tempty + kPiAcc;
+  uint64_t* aempty = afull + 1;
+  uint64_t* done = aempty + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + LY::TSLOT);
+  int* dead = reinterpret_cast<int*>(base + LY::DEAD);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const BatchDev bt = p.batch;
+  const int G = p.G, Q = bt.Q;
+  const int tpt = 128 / G;                 // query tokens per tile
+  const int tiles = (Q + tpt - 1) / tpt;
+  const int terms = p.iq_fp8 ? 1 : 2;
+
+  // this CTA's pairs [p0, p1)
+  long P = 0;
+  for (int s = 0; s < bt.S; ++s) P += (long)tiles * pi_seq_blocks(bt, s);
+  const long p0 = (long)blockIdx.x * P / gridDim.x, p1 = (long)(blockIdx.x + 1) * P / gridDim.x;
+  const int npairs = (int)(p1 - p0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPiStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);  // the MMA commit
+    }
+    for (int i = 0; i < kPiSStages; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 4);  // the pair's four epilogue warps
+    }
+    for (int i = 0; i < kPiAcc; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(afull, 8);
+    mbar_init(aempty, 1);
+    mbar_init(done, 1);
+    *dead = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tslot), kPiCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    // ---------------- key tiles and scales into the ring.  The block-table
+    // entries of 32 pairs at a time are read by the 32 lanes together.
+    PairCursor c;
+    pi_locate(bt, tiles, p0, c);
+    int issued = 0;
+    bool ok = true;
+    for (int j0 = 0; j0 < npairs && ok; j0 += 32) {
+      PairCursor cl = c;
+      pi_skip(bt, tiles, cl, lane);
+      const int my_phys = (j0 + lane < npairs) ? bt.row(cl.s)[cl.b] : -1;
+      const int my_qt = cl.qt;
+      for (int t = 0; t < 32 && j0 + t < npairs; ++t) {
+        const int phys = __shfl_sync(0xffffffffu, my_phys, t);
+        const int qt = __shfl_sync(0xffffffffu, my_qt, t);
+        const int j = j0 + t;
+        if (lane == 0) {
+          const int st = j % kPiStages, ss = j % kPiSStages;
+          if ((j >= kPiStages && !pi_wait(&kempty[st], (uint32_t)(((j / kPiStages) - 1) & 1), dead, p.status, 1)) ||
+              (j >= kPiSStages && !pi_wait(&sempty[ss], (uint32_t)(((j / kPiSStages) - 1) & 1), dead, p.status, 8))) {
+            ok = false;
+          } else {
+            uint8_t* kt = base + LY::KT + (size_t)st * kPiTile;
+            uint8_t* ks = base + LY::KS + (size_t)ss * kPiScales;
+            if (phys >= 0 && phys < p.num_blocks) {
+              fence_proxy_async();
+              mbar_expect_tx(&kfull[st], kPiTile);
+              tma_load_2d(kt, &tmap, 0, phys * kBlock, &kfull[st]);
+              mbar_expect_tx(&sfull[ss], kPiScales);
+              bulk_g2s(ks, p.idx_scale + (size_t)phys * kBlock, kPiScales, &sfull[ss]);
+            } else {
+              if (qt == 0) raise_flag(p.status, FLAG_BAD_BLOCK, phys);
+              // empty phases keep the rings in step; the epilogue writes -inf
+              mbar_arrive(&kfull[st]);
+              mbar_arrive(&sfull[ss]);
+            }
+            issued = j + 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      pi_skip(bt, tiles, c, 32);
+    }
+    // a CTA that gave up waits (bounded) for the copies it issued
+    if (lane == 0) {
+      for (int i = 0; i < kPiStages && i < issued; ++i) {
+        const int jj = issued - 1 - i;
+        mbar_wait(&kfull[jj % kPiStages], (uint32_t)((jj / kPiStages) & 1), 2000);
+      }
+      for (int i = 0; i < kPiSStages && i < issued; ++i) {
+        const int jj = issued - 1 - i;
+        mbar_wait(&sfull[jj % kPiSStages], (uint32_t)((jj / kPiSStages) & 1), 2000);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      PairCursor c;
+      pi_locate(bt, tiles, p0, c);
+      int a_use = 0, cur_tile = -1, cur_s = -1;
+      const uint32_t a0 = smem_u32(base + LY::A);
+      for (int j = 0; j < npairs; ++j) {
+        if (c.qt != cur_tile || c.s != cur_s) {
+          if (!pi_wait(afull, (uint32_t)(a_use & 1), dead, p.status, 2)) break;
+          ++a_use;
+          cur_tile = c.qt;
+          cur_s = c.s;
+        }
+        const int st = j % kPiStages, ab = j % kPiAcc;
+        if (!pi_wait(&kfull[st], (uint32_t)((j / kPiStages) & 1), dead, p.status, 3)) break;
+        if (j >= kPiAcc && !pi_wait(&tempty[ab], (uint32_t)(((j / kPiAcc) - 1) & 1), dead, p.status, 4)) break;
+        tc_fence_after();
+        const uint32_t bt0 = smem_u32(base + LY::KT + (size_t)st * kPiTile);
+        const uint32_t d = tmem + (uint32_t)(ab * 128);
+#pragma unroll 1
+        for (int term = 0; term < terms; ++term)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8(d, sw128_desc(a0 + term * kPiTile + 32 * k), sw128_desc(bt0 + 32 * k), kIdescF8,
+                   (term | k) != 0);
+        mma_commit(&tfull[ab]);
+        mma_commit(&kempty[st]);
+        pi_advance(bt, tiles, c);
+        if (j + 1 == npairs || c.qt != cur_tile || c.s != cur_s) mma_commit(aempty);  // the query tile is free
+      }
+      mma_commit(done);
+      mbar_wait(done, 0, 200000);
+    }
+  } else {
+    // ---------------- query tiles + epilogue (thread = accumulator row)
+    const int quarter = warp & 3;          // TMEM lanes 32 * quarter .. + 31
+    const int group = (warp - 2) >> 2;     // takes the pairs j with j % 2 == group
+    const int m = 32 * quarter + lane;     // row of the tile: token m / G, group m % G
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    PairCursor c;
+    pi_locate(bt, tiles, p0, c);
+    int a_use = 0, cur_tile = -1, cur_s = -1;
+    int T = 0, pos = -1;
+    bool row_ok = false;
+    float rowf = 0.f;
+    float* prow = nullptr;
+    for (int j = 0; j < npairs; ++j) {
+      if (c.qt != cur_tile || c.s != cur_s) {
+        // the MMAs of the previous tile must be done before its operand is overwritten
+        if (a_use > 0 && !pi_wait(aempty, (uint32_t)((a_use - 1) & 1), dead, p.status, 5)) break;
+        cur_tile = c.qt;
+        cur_s = c.s;
+        const int i = cur_tile * tpt + m / G, g = m % G;
+        T = bt.seq_len(cur_s);
+        row_ok = i < Q;
+        pos = T - Q + i;
+        prow = p.pooled + ((size_t)(cur_s * Q + i) * G + g) * bt.max_nb;
+        // this row of the operand: hi (and lo) e4m3, 16-byte chunks swizzled by row
+        uint8_t* ahi = base + LY::A + (size_t)m * 128;
+        uint8_t* alo = ahi + kPiTile;
+        const size_t qoff = ((size_t)(cur_s * Q + i) * G + g) * kDim;
+        if (p.iq_fp8) {
+          const uint8_t* src = static_cast<const uint8_t*>(p.index_q) + qoff;
+#pragma unroll
+          for (int ch = 0; ch < 8 && group == 0; ++ch) {
+            const uint4 v = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * ch) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(ahi + ((ch ^ (m & 7)) << 4)) = v;
+          }
+          rowf = p.iq_scale * p.col_const;
+        } else {
+          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.index_q) + qoff;
+          float amax = 0.f;
+          for (int ch = 0; ch < 16; ++ch) {
+            const uint4 v = row_ok ? *reinterpret_cast<const uint4*>(src + 8 * ch) : make_uint4(0, 0, 0, 0);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(h[e]);
+              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+          }
+          const int ex = pow2_fit(amax, 448.f);
+          const float ps = ldexpf(1.f, ex);
+          rowf = ldexpf(1.f, -ex) * p.col_const;
+          for (int ch = 0; ch < 8; ++ch) {  // 16 dims a chunk
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint4 v = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * ch + 8 * half) : make_uint4(0, 0, 0, 0);
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+              for (int e = 0; e < 4; e += 2) {
+                const float2 f0 = __bfloat1622float2(h[e]), f1 = __bfloat1622float2(h[e + 1]);
+                float h0, l0, h1, l1, h2, l2, h3, l3;
+                split_e4m3(f0.x * ps, h0, l0);
+                split_e4m3(f0.y * ps, h1, l1);
+                split_e4m3(f1.x * ps, h2, l2);
+                split_e4m3(f1.y * ps, h3, l3);
+                hw[2 * half + e / 2] = (uint32_t)pack_e4m3x2(h0, h1) | ((uint32_t)pack_e4m3x2(h2, h3) << 16);
+                lw[2 * half + e / 2] = (uint32_t)pack_e4m3x2(l0, l1) | ((uint32_t)pack_e4m3x2(l2, l3) << 16);
+              }
+            }
+            if (group == 0) *reinterpret_cast<uint4*>(ahi + ((ch ^ (m & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            else *reinterpret_cast<uint4*>(alo + ((ch ^ (m & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+        fence_proxy_async();  // the MMA reads the operand through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull);
+        ++a_use;
+      }
+      if ((j & 1) != group) {  // the other group's pair
+        pi_advance(bt, tiles, c);
+        continue;
+      }
+      const int ab = j % kPiAcc;
+      const int phys = bt.row(c.s)[c.b];  // used at the end: its latency hides behind the wait
+      if (!pi_wait(&tfull[ab], (uint32_t)((j / kPiAcc) & 1), dead, p.status, 6)) break;
+      // the pair's key scales (their own ring: the slot is not reused before
+      // this group releases it)
+      const int ss = j % kPiSStages;
+      if (!pi_wait(&sfull[ss], (uint32_t)((j / kPiSStages) & 1), dead, p.status, 7)) break;
+      tc_fence_after();
+      float mx = -INFINITY;
+      const float* ks = reinterpret_cast<const float*>(base + LY::KS + (size_t)ss * kPiScales);
+      const int key0 = c.b * kBlock;
+      const bool full_vis = key0 + kBlock - 1 <= pos;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {  // 64 columns: two loads in flight, one wait
+        float v[2][32];
+        tmem_ld32(lane_addr + (uint32_t)(ab * 128 + 64 * half), v[0]);
+        tmem_ld32(lane_addr + (uint32_t)(ab * 128 + 64 * half + 32), v[1]);
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[ab]);  // the accumulator may be overwritten
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int n0 = 64 * half + 32 * q;
+          if (full_vis) {
+            const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
+#pragma unroll
+            for (int n = 0; n < 32; n += 8) {
+              const float4 ka = k4[n >> 2], kb = k4[(n >> 2) + 1];
+              const float2 p0 = mul2(v[q][n], v[q][n + 1], ka.x, ka.y);
+              const float2 p1 = mul2(v[q][n + 2], v[q][n + 3], ka.z, ka.w);
+              const float2 p2 = mul2(v[q][n + 4], v[q][n + 5], kb.x, kb.y);
+              const float2 p3 = mul2(v[q][n + 6], v[q][n + 7], kb.z, kb.w);
+              m4[0] = max3(m4[0], p0.x, p0.y);
+              m4[1] = max3(m4[1], p1.x, p1.y);
+              m4[2] = max3(m4[2], p2.x, p2.y);
+              m4[3] = max3(m4[3], p3.x, p3.y);
+            }
+          } else {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              const float sc = (key0 + n0 + n <= pos) ? v[q][n] * ks[n0 + n] : -INFINITY;
+              m4[n & 3] = fmaxf(m4[n & 3], sc);
+            }
+          }
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[ss]);  // done with the scales
+      if (row_ok) prow[c.b] = (phys >= 0 && phys < p.num_blocks) ? mx * rowf : -INFINITY;
+      pi_advance(bt, tiles, c);
+    }
+  }
+
+  // blocks that hold no key of a sequence (past its length, or all of a
+  // malformed sequence): -inf for every (token, group) row, a row per warp
+  {
+    const long rows = (long)bt.S * Q * G;
+    const long nw = (long)gridDim.x * (kPiThreads / 32);
+    for (long row = (long)blockIdx.x * (kPiThreads / 32) + warp; row < rows; row += nw) {
+      const int nb = pi_seq_blocks(bt, (int)(row / ((long)Q * G)));
+      float* pr = p.pooled + row * bt.max_nb;
+      for (int b = nb + lane; b < bt.max_nb; b += 32) pr[b] = -INFINITY;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int s = 0; s < bt.S; ++s)
+      if (pi_seq_blocks(bt, s) == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
+  }
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kPiCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexerParams& p, int num_sms,
+                                   cudaStream_t st) {
+  const size_t smem = PiLayout::SMEM;
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(pindexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(pindexer_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pindexer_kernel, kPiThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    per_sm = 1;  // all 512 TMEM columns: one CTA per SM
+  }
+  const int grid = per_sm * (num_sms > 0 ? num_sms : 1);
+  pindexer_kernel<<<grid, kPiThreads, smem, st>>>(*tmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,69 @@
+"""The indexer of prefill chunks (more than 8 new tokens per sequence, FP8
+index cache), which runs on the tcgen05 tensor cores with the query tokens
+as the MMA's M side, against the oracle's pooled scores (MiniMax Sparse
+Attention model page, "Lightning indexer"; vLLM Day-0 blog, MSA indexer
+prefill).  The cases cover one and several 128-row query tiles, ragged last
+tiles, several sequences of different lengths, e4m3 index queries (one MMA
+term instead of the bf16 hi + lo pair), 1 / 2 / 4 / 8 groups (128, 64, 32, 16
+tokens a tile) and a bad block-table entry.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_03_gb300 as msa
+import msa_synth as ms
+from oracle import msa_oracle as O
+
+from _helpers import bind, check_pooled, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+def _pooled(c, w):
+    cfg = msa.default_config(w.topk)
+    cache, batch, iq, _ = bind(c)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    pooled = torch.full((w.num_seqs * w.q_per_seq, w.num_kv_heads, w.max_blocks), 7.0, dtype=torch.float32,
+                        device="cuda")
+    msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    return pooled.cpu().numpy(), st, flags
+
+
+def _oracle(c, w):
+    h = ms.case_to_host(c)
+    return np.concatenate([O.pooled_scores(h, s, w.index_dim ** -0.5) for s in range(w.num_seqs)])
+
+
+CASES = [
+    dict(seq_lens=(2000 + 64,), q_per_seq=64),
+    dict(seq_lens=(1500, 900), q_per_seq=24),
+    dict(seq_lens=(5000, 130, 4000), q_per_seq=100),
+    dict(seq_lens=(3000,), q_per_seq=40, q_dtype="fp8"),
+    dict(seq_lens=(2500,), q_per_seq=48, num_kv_heads=8),
+    dict(seq_lens=(2500,), q_per_seq=80, num_kv_heads=2),
+    dict(seq_lens=(1200,), q_per_seq=128, num_kv_heads=1),
+]
+
+
+@pytest.mark.parametrize("over", CASES)
+def test_prefill_indexer_matches_oracle(over):
+    w = ms.make_workload("fp8_prefill", seed=81, **over)
+    c = ms.make_case(w, device="cuda")
+    got, st, flags = _pooled(c, w)
+    assert st == 0, (msa.msa_status_string(st), flags)
+    check_pooled(got, _oracle(c, w))
+
+
+def test_prefill_indexer_bad_block_flags_and_skips():
+    w = ms.make_workload("fp8_prefill", seed=82, seq_lens=(1000,), q_per_seq=32)
+    c = ms.make_case(w, device="cuda")
+    ref = _oracle(c, w)
+    c["block_table"][0, 2] = c["num_blocks"] + 5
+    got, st, flags = _pooled(c, w)
+    assert st != 0 and flags & 1  # a block-table entry outside the pool
+    assert np.isneginf(got[:, :, 2]).all()
+    keep = [b for b in range(w.max_blocks) if b != 2]
+    check_pooled(got[:, :, keep], ref[:, :, keep])
