@@ -8,21 +8,23 @@
 //                   (index_q[s, i, g] . ik[t]) * kscale[t],
 // -inf where block b holds no visible key.  With thousands of new tokens the
 // contraction is dense, so the queries become the MMA's M side:
-//   D[128 x 128] = A[128 rows = (token, group)] x B[128 keys of one block]^T
-// with K = 128 index dims in four k32 steps of kind::f8f6f4 (e4m3 x e4m3).  A
+//   D[128 x 256] = A[128 rows = (token, group)] x B[256 keys of two blocks]^T
+// with K = 128 index dims in four k32 steps of kind::f8f6f4 (e4m3 x e4m3); an
+// M = 128 instruction costs about the same at N = 128 as at N = 256 on this
+// part, so each MMA takes two key blocks.  A
 // bf16 index query is scaled by a power of two per row (exact) and split into
 // e4m3 hi + lo terms that accumulate into the same TMEM columns, carrying all 8
 // significant bits of bf16; an e4m3 index query enters as is.
 //
-// One CTA (10 warps, persistent, one per SM) walks a contiguous run of
-// (query tile, key block) pairs:
-//   warp 0   copies key tiles (TMA, 128-byte swizzle) into a 10-stage ring
-//            (enough bytes in flight to cover L2 latency at the MMA rate), freed
-//            by the MMAs' completion, and their per-token scales into a 16-slot
-//            ring freed by the epilogue;
-//   warp 1   owns the SM's 512 TMEM columns (four 128-column accumulators); one
+// One CTA (10 warps, persistent, one per SM) walks a contiguous run of units
+// (query tile, two key blocks):
+//   warp 0   copies key tiles (TMA, 128-byte swizzle) into a 5-stage ring of
+//            two-tile stages (enough bytes in flight to cover L2 latency at the
+//            MMA rate), freed by the MMAs' completion, and their per-token
+//            scales into a 16-slot ring freed by the epilogue;
+//   warp 1   owns the SM's 512 TMEM columns (two 256-column accumulators); one
 //            thread issues the MMAs and commits them to mbarriers;
-//   warps 2-9 two groups of four, taking alternate pairs; each thread owns one
+//   warps 2-9 two groups of four, taking alternate units; each thread owns one
 //            accumulator row (tcgen05.ld 32x32b), multiplies by the key scales
 //            (packed f32x2), masks the keys its token cannot see, takes the max
 //            (three-input max) and writes P.  At each new query tile both
@@ -37,19 +39,21 @@ namespace msa {
 
 namespace {
 
-constexpr int kPiStages = 10;                  // key tiles in flight: L2 latency x the MMA rate
+constexpr int kPiStages = 5;                   // units (two key tiles) in flight: L2 latency x the MMA rate
 constexpr int kPiSStages = 16;                 // key-scale slots (released by the epilogue, which lags)
-constexpr int kPiAcc = 4;                      // accumulators of 128 columns
-constexpr int kPiCols = 128 * kPiAcc;          // TMEM columns (all 512 of the SM: one CTA per SM)
+constexpr int kPiAcc = 2;                      // accumulators of 256 columns (two key blocks)
+constexpr int kPiCols = 256 * kPiAcc;          // TMEM columns (all 512 of the SM: one CTA per SM)
 constexpr int kPiThreads = 320;                // producer, MMA, 2 x 4 epilogue warps
 constexpr uint32_t kPiTile = 128 * 128;        // bytes of one e4m3 128 x 128 tile
+constexpr uint32_t kPiStage = 2 * kPiTile;     // a unit's two key tiles, one 256-row operand
 constexpr uint32_t kPiScales = 128 * 4;        // fp32 key scales of one block
+constexpr uint32_t kPiSSlot = 2 * kPiScales;
 
 struct PiLayout {
   static constexpr uint32_t A = 0;                                  // [2 terms][16 KB]
-  static constexpr uint32_t KT = 2 * kPiTile;                       // [stages][16 KB]
-  static constexpr uint32_t KS = KT + kPiStages * kPiTile;          // [scale slots][512 B]
-  static constexpr uint32_t BARS = KS + kPiSStages * kPiScales;     // mbarriers
+  static constexpr uint32_t KT = 2 * kPiTile;                       // [stages][32 KB]
+  static constexpr uint32_t KS = KT + kPiStages * kPiStage;         // [scale slots][1 KB]
+  static constexpr uint32_t BARS = KS + kPiSStages * kPiSSlot;      // mbarriers
   // kfull, kempty, sfull, sempty, tfull, tempty, afull, aempty, done
   static constexpr uint32_t NBARS = 2 * kPiStages + 2 * kPiSStages + 2 * kPiAcc + 3;
   static constexpr uint32_t TSLOT = BARS + NBARS * 8;               // TMEM base from the allocator
@@ -131,17 +135,20 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor: D fp32, A and B e4m3, both K-major, N = 128, M = 128.
-constexpr uint32_t kIdescF8 = (1u << 4) | (0u << 7) | (0u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// Instruction descriptor: D fp32, A and B e4m3, both K-major, N = 256, M = 128.
+constexpr uint32_t kIdescF8 = (1u << 4) | (0u << 7) | (0u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 
 // ---------------------------------------------------------------- work walk
 
-// The pairs (sequence, query tile, key block) in order: sequence-major, then
-// tile, then block.  A sequence contributes tiles x (blocks that hold keys);
-// a malformed one (length outside [Q, max_blocks * 128]) none.
+// The work units (sequence, query tile, key-block pair) in order:
+// sequence-major, then tile, then pair.  Unit u of a tile covers key blocks 2u
+// and 2u + 1 (the second absent when the sequence has an odd block count).  A
+// sequence contributes tiles x ceil(blocks / 2) units; a malformed one (length
+// outside [Q, max_blocks * 128]) none.
 struct PairCursor {
-  int s, qt, b;
-  int nb;  // blocks of sequence s (kept so that walking reads no memory)
+  int s, qt, b;  // b: the unit within the tile
+  int nb;        // units of sequence s (kept so that walking reads no memory)
+  int nblk;      // key blocks of sequence s
 };
 
 __device__ __forceinline__ int pi_seq_blocks(const BatchDev& bt, int s) {
@@ -152,13 +159,15 @@ __device__ __forceinline__ int pi_seq_blocks(const BatchDev& bt, int s) {
 
 __device__ __forceinline__ void pi_locate(const BatchDev& bt, int tiles, long p, PairCursor& c) {
   c.s = bt.S;
-  c.qt = c.b = c.nb = 0;
+  c.qt = c.b = c.nb = c.nblk = 0;
   for (int s = 0; s < bt.S; ++s) {
-    const int nb = pi_seq_blocks(bt, s);
+    const int nblk = pi_seq_blocks(bt, s);
+    const int nb = (nblk + 1) / 2;
     const long n = (long)tiles * nb;
     if (p < n) {
       c.s = s;
       c.nb = nb;
+      c.nblk = nblk;
       c.qt = (int)(p / nb);
       c.b = (int)(p % nb);
       return;
@@ -174,9 +183,10 @@ __device__ __forceinline__ void pi_skip(const BatchDev& bt, int tiles, PairCurso
     c.b -= c.nb;
     if (++c.qt < tiles) continue;
     c.qt = 0;
-    c.nb = 0;
+    c.nb = c.nblk = 0;
     while (++c.s < bt.S) {
-      c.nb = pi_seq_blocks(bt, c.s);
+      c.nblk = pi_seq_blocks(bt, c.s);
+      c.nb = (c.nblk + 1) / 2;
       if (c.nb > 0) break;
     }
   }
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
 
   // this CTA's pairs [p0, p1)
   long P = 0;
-  for (int s = 0; s < bt.S; ++s) P += (long)tiles * pi_seq_blocks(bt, s);
+  for (int s = 0; s < bt.S; ++s) P += (long)tiles * ((pi_seq_blocks(bt, s) + 1) / 2);
   const long p0 = (long)blockIdx.x * P / gridDim.x, p1 = (long)(blockIdx.x + 1) * P / gridDim.x;
   const int npairs = (int)(p1 - p0);
 
@@ -231,7 +241,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
     }
     for (int i = 0; i < kPiSStages; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 4);  // the pair's four epilogue warps
+      mbar_init(&sempty[i], 4);  // the unit's four epilogue warps
     }
     for (int i = 0; i < kPiAcc; ++i) {
       mbar_init(&tfull[i], 1);
@@ -260,10 +270,14 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
     for (int j0 = 0; j0 < npairs && ok; j0 += 32) {
       PairCursor cl = c;
       pi_skip(bt, tiles, cl, lane);
-      const int my_phys = (j0 + lane < npairs) ? bt.row(cl.s)[cl.b] : -1;
+      // physical blocks of this lane's unit (-2: no second block)
+      const bool mine = j0 + lane < npairs;
+      const int my_ph0 = mine ? bt.row(cl.s)[2 * cl.b] : -1;
+      const int my_ph1 = (mine && 2 * cl.b + 1 < cl.nblk) ? bt.row(cl.s)[2 * cl.b + 1] : -2;
       const int my_qt = cl.qt;
       for (int t = 0; t < 32 && j0 + t < npairs; ++t) {
-        const int phys = __shfl_sync(0xffffffffu, my_phys, t);
+        const int ph0 = __shfl_sync(0xffffffffu, my_ph0, t);
+        const int ph1 = __shfl_sync(0xffffffffu, my_ph1, t);
         const int qt = __shfl_sync(0xffffffffu, my_qt, t);
         const int j = j0 + t;
         if (lane == 0) {
@@ -272,17 +286,24 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
               (j >= kPiSStages && !pi_wait(&sempty[ss], (uint32_t)(((j / kPiSStages) - 1) & 1), dead, p.status, 8))) {
             ok = false;
           } else {
-            uint8_t* kt = base + LY::KT + (size_t)st * kPiTile;
-            uint8_t* ks = base + LY::KS + (size_t)ss * kPiScales;
-            if (phys >= 0 && phys < p.num_blocks) {
+            uint8_t* kt = base + LY::KT + (size_t)st * kPiStage;
+            uint8_t* ks = base + LY::KS + (size_t)ss * kPiSSlot;
+            const bool v0 = ph0 >= 0 && ph0 < p.num_blocks;
+            const bool v1 = ph1 >= 0 && ph1 < p.num_blocks;
+            if (qt == 0 && !v0) raise_flag(p.status, FLAG_BAD_BLOCK, ph0);
+            if (qt == 0 && ph1 != -2 && !v1) raise_flag(p.status, FLAG_BAD_BLOCK, ph1);
+            // a block that is absent or rejected is not copied (its half of the
+            // operand keeps stale bytes, its scores are not used); a unit with
+            // nothing to copy completes its phases by plain arrivals
+            if (v0 || v1) {
               fence_proxy_async();
-              mbar_expect_tx(&kfull[st], kPiTile);
-              tma_load_2d(kt, &tmap, 0, phys * kBlock, &kfull[st]);
-              mbar_expect_tx(&sfull[ss], kPiScales);
-              bulk_g2s(ks, p.idx_scale + (size_t)phys * kBlock, kPiScales, &sfull[ss]);
+              mbar_expect_tx(&kfull[st], (v0 ? kPiTile : 0u) + (v1 ? kPiTile : 0u));
+              if (v0) tma_load_2d(kt, &tmap, 0, ph0 * kBlock, &kfull[st]);
+              if (v1) tma_load_2d(kt + kPiTile, &tmap, 0, ph1 * kBlock, &kfull[st]);
+              mbar_expect_tx(&sfull[ss], (v0 ? kPiScales : 0u) + (v1 ? kPiScales : 0u));
+              if (v0) bulk_g2s(ks, p.idx_scale + (size_t)ph0 * kBlock, kPiScales, &sfull[ss]);
+              if (v1) bulk_g2s(ks + kPiScales, p.idx_scale + (size_t)ph1 * kBlock, kPiScales, &sfull[ss]);
             } else {
-              if (qt == 0) raise_flag(p.status, FLAG_BAD_BLOCK, phys);
-              // empty phases keep the rings in step; the epilogue writes -inf
               mbar_arrive(&kfull[st]);
               mbar_arrive(&sfull[ss]);
             }
@@ -323,8 +344,8 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         if (!pi_wait(&kfull[st], (uint32_t)((j / kPiStages) & 1), dead, p.status, 3)) break;
         if (j >= kPiAcc && !pi_wait(&tempty[ab], (uint32_t)(((j / kPiAcc) - 1) & 1), dead, p.status, 4)) break;
         tc_fence_after();
-        const uint32_t bt0 = smem_u32(base + LY::KT + (size_t)st * kPiTile);
-        const uint32_t d = tmem + (uint32_t)(ab * 128);
+        const uint32_t bt0 = smem_u32(base + LY::KT + (size_t)st * kPiStage);
+        const uint32_t d = tmem + (uint32_t)(ab * 256);
 #pragma unroll 1
         for (int term = 0; term < terms; ++term)
 #pragma unroll
@@ -342,7 +363,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
   } else {
     // ---------------- query tiles + epilogue (thread = accumulator row)
     const int quarter = warp & 3;          // TMEM lanes 32 * quarter .. + 31
-    const int group = (warp - 2) >> 2;     // takes the pairs j with j % 2 == group
+    const int group = (warp - 2) >> 2;     // takes the units j with j % 2 == group
     const int m = 32 * quarter + lane;     // row of the tile: token m / G, group m % G
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     PairCursor c;
@@ -417,64 +438,75 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         if (lane == 0) mbar_arrive(afull);
         ++a_use;
       }
-      if ((j & 1) != group) {  // the other group's pair
+      if ((j & 1) != group) {  // the other group's unit
         pi_advance(bt, tiles, c);
         continue;
       }
       const int ab = j % kPiAcc;
-      const int phys = bt.row(c.s)[c.b];  // used at the end: its latency hides behind the wait
+      const int nblocks = (2 * c.b + 1 < c.nblk) ? 2 : 1;  // the unit's key blocks
+      // physical blocks, used at the end: their latency hides behind the waits
+      const int ph0 = bt.row(c.s)[2 * c.b];
+      const int ph1 = nblocks == 2 ? bt.row(c.s)[2 * c.b + 1] : -1;
       if (!pi_wait(&tfull[ab], (uint32_t)((j / kPiAcc) & 1), dead, p.status, 6)) break;
-      // the pair's key scales (their own ring: the slot is not reused before
+      // the unit's key scales (their own ring: the slot is not reused before
       // this group releases it)
       const int ss = j % kPiSStages;
       if (!pi_wait(&sfull[ss], (uint32_t)((j / kPiSStages) & 1), dead, p.status, 7)) break;
       tc_fence_after();
-      float mx = -INFINITY;
-      const float* ks = reinterpret_cast<const float*>(base + LY::KS + (size_t)ss * kPiScales);
-      const int key0 = c.b * kBlock;
-      const bool full_vis = key0 + kBlock - 1 <= pos;
+      float mxs[2] = {-INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {  // 64 columns: two loads in flight, one wait
-        float v[2][32];
-        tmem_ld32(lane_addr + (uint32_t)(ab * 128 + 64 * half), v[0]);
-        tmem_ld32(lane_addr + (uint32_t)(ab * 128 + 64 * half + 32), v[1]);
-        tmem_ld_wait();
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[ab]);  // the accumulator may be overwritten
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int h = 0; h < nblocks; ++h) {  // warp-uniform: the unit is the same for the whole warp
+        const float* ks = reinterpret_cast<const float*>(base + LY::KS + (size_t)ss * kPiSSlot) + 128 * h;
+        const int key0 = (2 * c.b + h) * kBlock;
+        const bool full_vis = key0 + kBlock - 1 <= pos;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {  // 64 columns: two loads in flight, one wait
+          float v[2][32];
+          const uint32_t col = (uint32_t)(ab * 256 + 128 * h + 64 * half);
+          tmem_ld32(lane_addr + col, v[0]);
+          tmem_ld32(lane_addr + col + 32, v[1]);
+          tmem_ld_wait();
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int n0 = 64 * half + 32 * q;
-          if (full_vis) {
-            const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
+          for (int q = 0; q < 2; ++q) {
+            const int n0 = 64 * half + 32 * q;
+            if (full_vis) {
+              const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
 #pragma unroll
-            for (int n = 0; n < 32; n += 8) {
-              const float4 ka = k4[n >> 2], kb = k4[(n >> 2) + 1];
-              const float2 p0 = mul2(v[q][n], v[q][n + 1], ka.x, ka.y);
-              const float2 p1 = mul2(v[q][n + 2], v[q][n + 3], ka.z, ka.w);
-              const float2 p2 = mul2(v[q][n + 4], v[q][n + 5], kb.x, kb.y);
-              const float2 p3 = mul2(v[q][n + 6], v[q][n + 7], kb.z, kb.w);
-              m4[0] = max3(m4[0], p0.x, p0.y);
-              m4[1] = max3(m4[1], p1.x, p1.y);
-              m4[2] = max3(m4[2], p2.x, p2.y);
-              m4[3] = max3(m4[3], p3.x, p3.y);
-            }
-          } else {
+              for (int n = 0; n < 32; n += 8) {
+                const float4 ka = k4[n >> 2], kb = k4[(n >> 2) + 1];
+                const float2 p0 = mul2(v[q][n], v[q][n + 1], ka.x, ka.y);
+                const float2 p1 = mul2(v[q][n + 2], v[q][n + 3], ka.z, ka.w);
+                const float2 p2 = mul2(v[q][n + 4], v[q][n + 5], kb.x, kb.y);
+                const float2 p3 = mul2(v[q][n + 6], v[q][n + 7], kb.z, kb.w);
+                m4[0] = max3(m4[0], p0.x, p0.y);
+                m4[1] = max3(m4[1], p1.x, p1.y);
+                m4[2] = max3(m4[2], p2.x, p2.y);
+                m4[3] = max3(m4[3], p3.x, p3.y);
+              }
+            } else {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-              const float sc = (key0 + n0 + n <= pos) ? v[q][n] * ks[n0 + n] : -INFINITY;
-              m4[n & 3] = fmaxf(m4[n & 3], sc);
+              for (int n = 0; n < 32; ++n) {
+                const float sc = (key0 + n0 + n <= pos) ? v[q][n] * ks[n0 + n] : -INFINITY;
+                m4[n & 3] = fmaxf(m4[n & 3], sc);
+              }
             }
           }
+          mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
         }
-        mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        mxs[h] = mx;
       }
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[ss]);  // done with the scales
-      if (row_ok) prow[c.b] = (phys >= 0 && phys < p.num_blocks) ? mx * rowf : -INFINITY;
+      if (lane == 0) {
+        mbar_arrive(&tempty[ab]);  // the accumulator may be overwritten
+        mbar_arrive(&sempty[ss]);  // done with the scales
+      }
+      if (row_ok) {
+        prow[2 * c.b] = (ph0 >= 0 && ph0 < p.num_blocks) ? mxs[0] * rowf : -INFINITY;
+        if (nblocks == 2) prow[2 * c.b + 1] = (ph1 >= 0 && ph1 < p.num_blocks) ? mxs[1] * rowf : -INFINITY;
+      }
       pi_advance(bt, tiles, c);
     }
   }
