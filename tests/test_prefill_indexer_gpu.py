@@ -67,3 +67,34 @@ def test_prefill_indexer_bad_block_flags_and_skips():
     assert np.isneginf(got[:, :, 2]).all()
     keep = [b for b in range(w.max_blocks) if b != 2]
     check_pooled(got[:, :, keep], ref[:, :, keep])
+
+
+@pytest.mark.parametrize("over", [dict(seq_lens=(3000, 1700), q_per_seq=40, num_kv_heads=8),
+                                  dict(seq_lens=(2600,), q_per_seq=72, num_kv_heads=2),
+                                  dict(seq_lens=(2200,), q_per_seq=48, q_dtype="fp8")])
+def test_prefill_whole_path_matches_oracle(over):
+    # msa_decode end to end on a prefill chunk: tcgen05 indexer, top-k, per-token attend
+    from _helpers import check_out, check_selection, gpu_path
+    w = ms.make_workload("fp8_prefill", seed=83, **over)
+    c = ms.make_case(w, device="cuda")
+    g = gpu_path(c)
+    h = ms.case_to_host(c)
+    ref = _oracle(c, w)
+    check_selection(g["topk"], ref, w.seq_lens, w.q_per_seq, w.topk)
+    out = np.zeros_like(g["out"])
+    for s in range(w.num_seqs):
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+    check_out(g["out"], out)
+
+
+def test_prefill_indexer_bad_seq_len_flags_and_fills():
+    # a sequence shorter than its new tokens: flagged, its rows stay -inf, the other is scored
+    w = ms.make_workload("fp8_prefill", seed=84, seq_lens=(900, 700), q_per_seq=32)
+    c = ms.make_case(w, device="cuda")
+    ref = _oracle(c, w)
+    c["seq_lens"][1] = 20
+    got, st, flags = _pooled(c, w)
+    assert st != 0 and flags & 2
+    assert np.isneginf(got[32:]).all()
+    check_pooled(got[:32], ref[:32])
