@@ -36,9 +36,9 @@ WORKLOAD_TEXT = {
 }
 
 def kernels_per_step(q_per_seq: int) -> int:
-    """Launches of one msa_decode: indexer, top-k, attend, and a union kernel for
-    2 to 8 new tokens a sequence (a prefill chunk's attend runs per token)."""
-    return 4 if 1 < q_per_seq <= 8 else 3
+    """Launches of one msa_decode: indexer, top-k, attend (each new token its own
+    one-token sequence in the attend, whatever the count)."""
+    return 3
 
 
 def ncu_traffic(workload: str, kernel: str = "indexer"):

@@ -172,11 +172,11 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.chunks = b->q_per_seq / QV;
   pl.S = b->num_seqs * pl.chunks;
   pl.Q = QV;
-  // The attend of a prefill chunk runs every token as its own one-token
-  // sequence: neighbouring tokens' selections overlap little, so a union over
-  // 8 tokens would stream each block for 32 columns of which about 4 chose it.
-  // Up to 8 new tokens (speculative verify) share a union.
-  pl.Qa = b->q_per_seq > 8 ? 1 : QV;
+  // The attend runs every new token as its own one-token sequence (speculative
+  // verify and prefill chunks alike): the tokens' selections overlap little, so
+  // a union over 8 tokens streams each block for 32 query columns of which
+  // about 4 chose it, four times the work per block for the few blocks saved.
+  pl.Qa = 1;
   pl.chunks_a = b->q_per_seq / pl.Qa;
   pl.Sa = b->num_seqs * pl.chunks_a;
   const int Q = pl.Q, G = c->num_kv_heads;
