@@ -145,7 +145,7 @@ constexpr uint32_t kIdescF8 = (1u << 4) | (0u << 7) | (0u << 10) | ((256u >> 3) 
 // and 2u + 1 (the second absent when the sequence has an odd block count).  A
 // sequence contributes tiles x ceil(blocks / 2) units; a malformed one (length
 // outside [Q, max_blocks * 128]) none.
-struct PairCursor {
+struct UnitCursor {
   int s, qt, b;  // b: the unit within the tile
   int nb;        // units of sequence s (kept so that walking reads no memory)
   int nblk;      // key blocks of sequence s
@@ -157,7 +157,7 @@ __device__ __forceinline__ int pi_seq_blocks(const BatchDev& bt, int s) {
   return (T + kBlock - 1) / kBlock;
 }
 
-__device__ __forceinline__ void pi_locate(const BatchDev& bt, int tiles, long p, PairCursor& c) {
+__device__ __forceinline__ void pi_locate(const BatchDev& bt, int tiles, long p, UnitCursor& c) {
   c.s = bt.S;
   c.qt = c.b = c.nb = c.nblk = 0;
   for (int s = 0; s < bt.S; ++s) {
@@ -176,8 +176,8 @@ __device__ __forceinline__ void pi_locate(const BatchDev& bt, int tiles, long p,
   }
 }
 
-// k pairs further on (past the last pair: s = S)
-__device__ __forceinline__ void pi_skip(const BatchDev& bt, int tiles, PairCursor& c, int k) {
+// k units further on (past the last unit: s = S)
+__device__ __forceinline__ void pi_skip(const BatchDev& bt, int tiles, UnitCursor& c, int k) {
   c.b += k;
   while (c.s < bt.S && c.b >= c.nb) {
     c.b -= c.nb;
@@ -192,7 +192,7 @@ __device__ __forceinline__ void pi_skip(const BatchDev& bt, int tiles, PairCurso
   }
 }
 
-__device__ __forceinline__ void pi_advance(const BatchDev& bt, int tiles, PairCursor& c) { pi_skip(bt, tiles, c, 1); }
+__device__ __forceinline__ void pi_advance(const BatchDev& bt, int tiles, UnitCursor& c) { pi_skip(bt, tiles, c, 1); }
 
 __device__ __forceinline__ bool pi_wait(uint64_t* bar, uint32_t parity, int* dead, DeviceStatus* st, int where) {
   if (*reinterpret_cast<volatile int*>(dead)) return false;
@@ -228,11 +228,11 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
   const int tiles = (Q + tpt - 1) / tpt;
   const int terms = p.iq_fp8 ? 1 : 2;
 
-  // this CTA's pairs [p0, p1)
+  // this CTA's units [p0, p1)
   long P = 0;
   for (int s = 0; s < bt.S; ++s) P += (long)tiles * ((pi_seq_blocks(bt, s) + 1) / 2);
   const long p0 = (long)blockIdx.x * P / gridDim.x, p1 = (long)(blockIdx.x + 1) * P / gridDim.x;
-  const int npairs = (int)(p1 - p0);
+  const int nunits = (int)(p1 - p0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPiStages; ++i) {
@@ -262,20 +262,20 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
 
   if (warp == 0) {
     // ---------------- key tiles and scales into the ring.  The block-table
-    // entries of 32 pairs at a time are read by the 32 lanes together.
-    PairCursor c;
+    // entries of 32 units at a time are read by the 32 lanes together.
+    UnitCursor c;
     pi_locate(bt, tiles, p0, c);
     int issued = 0;
     bool ok = true;
-    for (int j0 = 0; j0 < npairs && ok; j0 += 32) {
-      PairCursor cl = c;
+    for (int j0 = 0; j0 < nunits && ok; j0 += 32) {
+      UnitCursor cl = c;
       pi_skip(bt, tiles, cl, lane);
       // physical blocks of this lane's unit (-2: no second block)
-      const bool mine = j0 + lane < npairs;
+      const bool mine = j0 + lane < nunits;
       const int my_ph0 = mine ? bt.row(cl.s)[2 * cl.b] : -1;
       const int my_ph1 = (mine && 2 * cl.b + 1 < cl.nblk) ? bt.row(cl.s)[2 * cl.b + 1] : -2;
       const int my_qt = cl.qt;
-      for (int t = 0; t < 32 && j0 + t < npairs; ++t) {
+      for (int t = 0; t < 32 && j0 + t < nunits; ++t) {
         const int ph0 = __shfl_sync(0xffffffffu, my_ph0, t);
         const int ph1 = __shfl_sync(0xffffffffu, my_ph1, t);
         const int qt = __shfl_sync(0xffffffffu, my_qt, t);
@@ -329,11 +329,11 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
   } else if (warp == 1) {
     // ---------------- MMA issue (one thread)
     if (lane == 0) {
-      PairCursor c;
+      UnitCursor c;
       pi_locate(bt, tiles, p0, c);
       int a_use = 0, cur_tile = -1, cur_s = -1;
       const uint32_t a0 = smem_u32(base + LY::A);
-      for (int j = 0; j < npairs; ++j) {
+      for (int j = 0; j < nunits; ++j) {
         if (c.qt != cur_tile || c.s != cur_s) {
           if (!pi_wait(afull, (uint32_t)(a_use & 1), dead, p.status, 2)) break;
           ++a_use;
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         mma_commit(&tfull[ab]);
         mma_commit(&kempty[st]);
         pi_advance(bt, tiles, c);
-        if (j + 1 == npairs || c.qt != cur_tile || c.s != cur_s) mma_commit(aempty);  // the query tile is free
+        if (j + 1 == nunits || c.qt != cur_tile || c.s != cur_s) mma_commit(aempty);  // the query tile is free
       }
       mma_commit(done);
       mbar_wait(done, 0, 200000);
@@ -366,14 +366,14 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
     const int group = (warp - 2) >> 2;     // takes the units j with j % 2 == group
     const int m = 32 * quarter + lane;     // row of the tile: token m / G, group m % G
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-    PairCursor c;
+    UnitCursor c;
     pi_locate(bt, tiles, p0, c);
     int a_use = 0, cur_tile = -1, cur_s = -1;
     int T = 0, pos = -1;
     bool row_ok = false;
     float rowf = 0.f;
     float* prow = nullptr;
-    for (int j = 0; j < npairs; ++j) {
+    for (int j = 0; j < nunits; ++j) {
       if (c.qt != cur_tile || c.s != cur_s) {
         // the MMAs of the previous tile must be done before its operand is overwritten
         if (a_use > 0 && !pi_wait(aempty, (uint32_t)((a_use - 1) & 1), dead, p.status, 5)) break;
