@@ -9,9 +9,9 @@
 // -inf where block b holds no visible key.  With thousands of new tokens the
 // contraction is dense, so the queries become the MMA's M side:
 //   D[128 x 256] = A[128 rows = (token, group)] x B[256 keys of two blocks]^T
-// with K = 128 index dims in four k32 steps of kind::f8f6f4 (e4m3 x e4m3); an
-// M = 128 instruction costs about the same at N = 128 as at N = 256 on this
-// part, so each MMA takes two key blocks.  A
+// with K = 128 index dims in four k32 steps of kind::f8f6f4 (e4m3 x e4m3);
+// two key blocks per MMA halve the per-unit costs that do not scale with N
+// (waits, commits, the accumulator hand-off to the epilogue).  A
 // bf16 index query is scaled by a power of two per row (exact) and split into
 // e4m3 hi + lo terms that accumulate into the same TMEM columns, carrying all 8
 // significant bits of bf16; an e4m3 index query enters as is.
