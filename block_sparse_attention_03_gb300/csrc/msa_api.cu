@@ -148,6 +148,10 @@ struct Plan {
   size_t off_status = 0, off_pooled = 0, off_uids = 0, off_umask = 0, off_ucount = 0, off_ctr = 0, off_qfa = 0,
          off_cfa = 0, off_po = 0, off_pml = 0, total = 0;
   int nctr = 0;             // attend counters: splits finished per (sequence, group)
+  // prefill chunks over an FP8 cache: the key-block-major attend (selection lists,
+  // one partial per (token, head, slot), a combine pass)
+  bool k2q = false;
+  size_t off_kcnt = 0, off_koff = 0, off_kcur = 0, off_kitem = 0, off_kent = 0, off_kpo = 0, off_kpml = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -206,6 +210,19 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
   pl.off_po = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 128 * 4);
   pl.off_pml = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 2 * 4);
+  pl.k2q = fa == FMT_FP8 && b->q_per_seq > 8 && (pl.r == 1 || pl.r == 2 || pl.r == 4 || pl.r == 8);
+  if (pl.k2q) {
+    const size_t L = (size_t)b->num_seqs * G * b->max_blocks_per_seq;
+    const size_t E = (size_t)b->num_seqs * b->q_per_seq * G * cfg->topk;
+    const size_t P = E * pl.r;
+    pl.off_kcnt = o; o = align256(o + L * 4);
+    pl.off_koff = o; o = align256(o + L * 4);
+    pl.off_kcur = o; o = align256(o + L * 4);
+    pl.off_kitem = o; o = align256(o + (L + 1) * 4);
+    pl.off_kent = o; o = align256(o + E * 4);
+    pl.off_kpo = o; o = align256(o + P * 128 * 4);
+    pl.off_kpml = o; o = align256(o + P * 2 * 4);
+  }
   pl.total = o;
   return MSA_OK;
 }
@@ -411,6 +428,47 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   return MSA_OK;
 }
 
+// The key-block-major attend of a prefill chunk from the selection topk_idx.
+msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* q,
+                     int hq, const int32_t* topk_idx, void* out, float* lse, const Plan& pl, void* ws,
+                     cudaStream_t st) {
+  const int G = c->num_kv_heads;
+  CUtensorMap tk, tv;
+  const long rows = (long)c->num_blocks * G * kBlock;
+  if (!encode_rows(&tk, c->k, rows, false) || !encode_rows(&tv, c->v, rows, false)) return MSA_ERR_CUDA;
+  Plan real;
+  real.S = b->num_seqs;
+  real.Q = b->q_per_seq;
+  real.chunks = 1;
+  K2qParams kp;
+  kp.batch = batch_dev(b, real);
+  kp.G = G;
+  kp.r = hq / G;
+  kp.topk = cfg->topk;
+  kp.num_blocks = c->num_blocks;
+  kp.topk_idx = topk_idx;
+  kp.cnt = at<int32_t>(ws, pl.off_kcnt);
+  kp.off = at<int32_t>(ws, pl.off_koff);
+  kp.cur = at<int32_t>(ws, pl.off_kcur);
+  kp.item_off = at<int32_t>(ws, pl.off_kitem);
+  kp.entries = at<int32_t>(ws, pl.off_kent);
+  kp.k_scale = c->k_scale;
+  kp.v_scale = c->v_scale;
+  kp.q = q->data;
+  kp.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
+  kp.q_scale = kp.q_fp8 ? q->scale : 1.f;
+  kp.col_const = cfg->sm_scale * 1.4426950408889634f;
+  kp.part_o = at<float>(ws, pl.off_kpo);
+  kp.part_ml = at<float>(ws, pl.off_kpml);
+  kp.out = out;
+  kp.lse = lse;
+  kp.status = at<DeviceStatus>(ws, pl.off_status);
+  if (launch_k2q_build(kp, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (launch_k2q_attend(&tk, &tv, kp, sm_count(), st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (launch_k2q_combine(kp, st) != cudaSuccess) return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -484,6 +542,7 @@ msa_status_t msa_sparse_attend(const msa_cache_t* cache, const msa_batch_t* batc
   Plan pl;
   if ((s = make_plan(cache, batch, cfg, num_q_heads, true, q->dtype == MSA_DTYPE_FP8_E4M3, pl)) != MSA_OK) return s;
   if (workspace_bytes < pl.total) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  if (pl.k2q) return run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, (cudaStream_t)stream);
   return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, (cudaStream_t)stream, false);
 }
 
@@ -503,6 +562,12 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, cons
   cudaStream_t st = (cudaStream_t)stream;
   float* pooled = at<float>(workspace, pl.off_pooled);
   if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st)) != MSA_OK) return s;
+  if (pl.k2q) {
+    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, false)) !=
+        MSA_OK)
+      return s;
+    return run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st);
+  }
   const FragJob fj = {cache, q, num_q_heads};
   if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, true,
                     pl.direct ? &fj : nullptr)) != MSA_OK)

@@ -157,7 +157,36 @@ struct PrefillIndexerParams {
   DeviceStatus* status;
 };
 
+// Key-block-major attend of prefill chunks (the selections inverted into one
+// list per (sequence, group, block) of the (token, slot) pairs that chose it).
+constexpr int kK2qTokens = 16;  // tokens per attend item (one K/V tile read for all of them)
+struct K2qParams {
+  BatchDev batch;            // the real batch: S sequences, Q new tokens each
+  int32_t G, r, topk;
+  int32_t num_blocks;
+  const int32_t* topk_idx;   // [S*Q][G][topk]
+  int32_t* cnt;              // [L = S*G*max_nb] pairs per list (zeroed before the count)
+  int32_t* off;              // [L] first entry of each list
+  int32_t* cur;              // [L] fill cursors
+  int32_t* item_off;         // [L + 1] first attend item of each list; [L] = items in all
+  int32_t* entries;          // [S*Q*G*topk] token * 32 + slot, list by list
+  const float* k_scale;      // FP8 per-token scales
+  const float* v_scale;
+  const void* q;             // [S*Q][G*r][128]
+  int32_t q_fp8;
+  float q_scale, col_const;
+  float* part_o;             // [S*Q*G*r*topk][128] per (token, head, slot)
+  float* part_ml;            // [S*Q*G*r*topk][2]
+  void* out;                 // bf16 [S*Q][G*r][128]
+  float* lse;
+  DeviceStatus* status;
+};
+
 // launchers (return cudaGetLastError())
+cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st);    // count, scan, fill
+cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_k2q_combine(const K2qParams& p, cudaStream_t st);
 cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexerParams& p, int num_sms,
                                    cudaStream_t st);
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,

@@ -1,0 +1,154 @@
+// Key-block-major attend of prefill chunks: the selection inverted into lists
+// (the model page's key -> query CSR, `build_k2q_csr`) and the per-token merge
+// of the per-block partials.
+//
+// Count: for every (token, group, slot) whose selected block is b, one more
+// entry in list (sequence, group, b).  Scan (one CTA): each list's first entry
+// and first attend item (kK2qTokens entries an item).  Fill: every entry
+// (token * 32 + slot) into its list, in arrival order (the per-entry results
+// do not depend on it).  The attend (msa_attend.cu) reads each item's K/V tile
+// once and writes one partial (o, m, l) per (token, head, slot); combine
+// merges a token's slots by log-sum-exp (MiniMax Sparse Attention model page,
+// "Top-k block selection": exact softmax over the union of the token's
+// selected blocks).
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+
+namespace {
+
+__global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
+  const BatchDev bt = p.batch;
+  const long n = (long)bt.S * bt.Q * p.G * p.topk;
+  for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
+    const int b = p.topk_idx[e];
+    if (b < 0 || b >= bt.max_nb) continue;
+    const long row = e / p.topk;  // token * G + g
+    const int s = (int)(row / ((long)bt.Q * p.G)), g = (int)(row % p.G);
+    atomicAdd(&p.cnt[((long)s * p.G + g) * bt.max_nb + b], 1);
+  }
+}
+
+// One CTA of 1024 threads: thread t owns the contiguous lists [t*L/1024, (t+1)*L/1024).
+__global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
+  __shared__ int se[1024], si[1024];
+  const BatchDev bt = p.batch;
+  const long L = (long)bt.S * p.G * bt.max_nb;
+  const int t = threadIdx.x;
+  const long l0 = t * L / 1024, l1 = (t + 1) * L / 1024;
+  int ne = 0, ni = 0;
+  for (long i = l0; i < l1; ++i) {
+    const int c = p.cnt[i];
+    ne += c;
+    ni += (c + kK2qTokens - 1) / kK2qTokens;
+  }
+  se[t] = ne;
+  si[t] = ni;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scans
+    const int ae = t >= o ? se[t - o] : 0, ai = t >= o ? si[t - o] : 0;
+    __syncthreads();
+    se[t] += ae;
+    si[t] += ai;
+    __syncthreads();
+  }
+  int e0 = se[t] - ne, i0 = si[t] - ni;
+  for (long i = l0; i < l1; ++i) {
+    const int c = p.cnt[i];
+    p.off[i] = e0;
+    p.cur[i] = e0;
+    p.item_off[i] = i0;
+    e0 += c;
+    i0 += (c + kK2qTokens - 1) / kK2qTokens;
+  }
+  if (t == 1023) p.item_off[L] = si[1023];
+}
+
+__global__ void __launch_bounds__(256) k2q_fill_kernel(const K2qParams p) {
+  const BatchDev bt = p.batch;
+  const long n = (long)bt.S * bt.Q * p.G * p.topk;
+  for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
+    const int b = p.topk_idx[e];
+    if (b < 0 || b >= bt.max_nb) continue;
+    const long row = e / p.topk;
+    const int slot = (int)(e % p.topk);
+    const long token = row / p.G;
+    const int s = (int)(token / bt.Q), g = (int)(row % p.G);
+    const int at = atomicAdd(&p.cur[((long)s * p.G + g) * bt.max_nb + b], 1);
+    p.entries[at] = (int)(token * 32 + slot);
+  }
+}
+
+__device__ __forceinline__ float k2q_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One warp per (token, head): lane l holds dims 4l .. 4l+3; the token's
+// selected slots merged by log-sum-exp in base 2 (m and l come that way).
+__global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
+  const BatchDev bt = p.batch;
+  const int H = p.G * p.r;
+  const long rows = (long)bt.S * bt.Q * H;
+  const int lane = threadIdx.x & 31;
+  const long nw = (long)gridDim.x * (blockDim.x >> 5);
+  for (long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+    const long token = row / H;
+    const int h = (int)(row % H), g = h / p.r;
+    const int32_t* sel = p.topk_idx + (token * p.G + g) * p.topk;
+    float M = -INFINITY, Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < p.topk; ++k) {
+      if (sel[k] < 0) continue;
+      const long part = row * p.topk + k;
+      const float m = __ldcg(p.part_ml + part * 2), l = __ldcg(p.part_ml + part * 2 + 1);
+      if (m == -INFINITY) continue;
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + part * 128) + lane);
+      const float mn = fmaxf(M, m);
+      const float a = k2q_ex2(M - mn), w = k2q_ex2(m - mn);  // M = -inf: a = 0
+      acc.x = acc.x * a + w * o.x;
+      acc.y = acc.y * a + w * o.y;
+      acc.z = acc.z * a + w * o.z;
+      acc.w = acc.w * a + w * o.w;
+      Lsum = Lsum * a + w * l;
+      M = mn;
+    }
+    const float inv = Lsum > 0.f ? __fdividef(1.f, Lsum) : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * 128 + 4 * lane) = pk;
+    if (lane == 0 && p.lse) p.lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st) {
+  const long L = (long)p.batch.S * p.G * p.batch.max_nb;
+  cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)L * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  const long n = (long)p.batch.S * p.batch.Q * p.G * p.topk;
+  long grid = (n + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  if (grid < 1) grid = 1;
+  k2q_count_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
+  k2q_scan_kernel<<<1, 1024, 0, st>>>(p);
+  k2q_fill_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_k2q_combine(const K2qParams& p, cudaStream_t st) {
+  const long rows = (long)p.batch.S * p.batch.Q * p.G * p.r;
+  long grid = (rows + 7) / 8;
+  if (grid > 65535) grid = 65535;
+  if (grid < 1) grid = 1;
+  k2q_combine_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace msa
