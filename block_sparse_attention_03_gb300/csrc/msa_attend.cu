@@ -1095,7 +1095,7 @@ struct K2qLayout {
   static constexpr size_t PSM = round_up(FR + FRW, 16);                     // per-warp P tiles
   static constexpr size_t PSM_WARP = 64 * 32;
   static constexpr size_t QO = PSM + 4 * PSM_WARP;                          // per-warp staging: q rows, then o
-  static constexpr size_t QO_WARP = 8 * 128 * 4;
+  static constexpr size_t QO_WARP = 8 * kMergeRow * 4;  // 8 q rows (padded) or 8 o rows of kMergeRow
   static constexpr size_t HDR = QO + 4 * QO_WARP;                           // [2] {n, s, g, b} + entries
   static constexpr size_t HDR_STAGE = 16 + kK2qTokens * 4;
   static constexpr size_t BARS = round_up(HDR + 2 * HDR_STAGE, 16);
@@ -1190,18 +1190,21 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       const int ncol = min(tpc, n - ch * tpc) * r;  // real columns of this tile
       // the tile's query rows into the warp's staging area with 16-byte loads
       // (row col = 128 elements), then this warp's fragments (tile ct = warp)
+      // rows padded by 32 bytes: the 8 rows of a fragment load then start 8
+      // banks apart
       uint8_t* qo = base + LY::QO + (size_t)warp * LY::QO_WARP;
       const int esz = p.q_fp8 ? 1 : 2;
-      const int chunks = 128 * esz / 16;  // 16-byte pieces a row
+      const int chunks = 128 * esz / 16;       // 16-byte pieces a row
+      const int qstride = 128 * esz + 32;      // bytes between staged rows
       for (int e = lane; e < ncol * chunks; e += 32) {
         const int col = e / chunks, pc = e % chunks;
         const long row = (long)(hdr[4 + ch * tpc + col / r] >> 5) * H + g * r + col % r;
-        *reinterpret_cast<uint4*>(qo + (size_t)col * 128 * esz + 16 * pc) =
+        *reinterpret_cast<uint4*>(qo + (size_t)col * qstride + 16 * pc) =
             *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + (size_t)row * 128 * esz + 16 * pc);
       }
       __syncwarp();
       long rows[1];
-      rows[0] = g8 < ncol ? (long)g8 * kDim : -1l;
+      rows[0] = g8 < ncol ? (long)g8 * (qstride / esz) : -1l;
       uint32_t bq[SP][1][TR::QKS][2];
       float cf[1][2];
       build_qfrag<FMT_FP8, 1, SP, TR::QKS>(qo, p.q_fp8 != 0, rows, p.q_scale, p.col_const, bq, cf, lane);
@@ -1233,8 +1236,9 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       attend_block<FMT_FP8, 4, SP>(stg, base + LY::PSM + (size_t)warp * LY::PSM_WARP, nullptr, fr, warp, colf, qlim,
                                    qbit, 1u, b * kBlock, 0, warp, lane, m_run, l_run, o, e_prev, kAllPhases);
       // the partial of every (token, head) column for this slot: o through the
-      // staging area (the query rows are no longer needed), then one 512-byte
-      // row a column
+      // staging area (the query rows are no longer needed) in accumulator-row
+      // order with padded rows (conflict-free stores), then one 512-byte row a
+      // column
       const float oscale = (e_prev >= -126 && e_prev <= 126) ? pow2i(-e_prev) : ldexpf(1.f, -e_prev);
       float* os = reinterpret_cast<float*>(qo);
 #pragma unroll
@@ -1247,10 +1251,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm)
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int d = 16 * (((g8 & 1) << 2) | (g8 >> 1)) + 2 * mm + h2;
-            os[col * 128 + d] = o[mm][c + 2 * h2] * oscale;
-          }
+          for (int h2 = 0; h2 < 2; ++h2) os[col * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
         if (g8 == 0 && col < ncol) {
           const int ent = hdr[4 + ch * tpc + col / r];
           const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
@@ -1262,7 +1263,14 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       for (int col = 0; col < ncol; ++col) {
         const int ent = hdr[4 + ch * tpc + col / r];
         const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
-        reinterpret_cast<float4*>(p.part_o + part * 128)[lane] = reinterpret_cast<const float4*>(os + col * 128)[lane];
+        float v4[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {  // dim d = 4 lane + t from its accumulator row
+          const int d = 4 * lane + t, q = d >> 4, rem = d & 15;
+          const int gg = ((q & 3) << 1) | (q >> 2);
+          v4[t] = os[col * kMergeRow + 16 * (rem >> 1) + 8 * (rem & 1) + gg];
+        }
+        reinterpret_cast<float4*>(p.part_o + part * 128)[lane] = make_float4(v4[0], v4[1], v4[2], v4[3]);
       }
       __syncwarp();
     }
