@@ -1145,7 +1145,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
     const int phys = bt.row(s)[b];
     const bool ok = phys >= 0 && phys < p.num_blocks && n > 0;
     int32_t* hdr = reinterpret_cast<int32_t*>(base + LY::HDR + (size_t)st * LY::HDR_STAGE);
-    hdr[0] = ok ? n : 0;
+    hdr[0] = ok ? n : -n;  // negative: the block is rejected, its entries get empty partials
     hdr[1] = s;
     hdr[2] = g;
     hdr[3] = b;
@@ -1161,7 +1161,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_scale + tile_id * kBlock, TR::VSC, &bars[st]);
     } else {
       if (n > 0) raise_flag(p.status, FLAG_BAD_BLOCK, phys);
-      mbar_arrive(&bars[st]);  // an empty phase: the item's partials stay unwritten, its slots skipped
+      mbar_arrive(&bars[st]);  // an empty phase
     }
   };
 
@@ -1185,6 +1185,14 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
     const int n = hdr[0], s = hdr[1], g = hdr[2], b = hdr[3];
     const int T = bt.seq_len(s);
     const uint8_t* stg = base + (size_t)st * LY::STAGE;
+    if (n < 0) {  // rejected block: m = -inf, so that the combine leaves these slots out
+      for (int e = tid; e < -n * r; e += kK2qThreads) {
+        const int ent = hdr[4 + e / r];
+        const long part = ((long)(ent >> 5) * H + g * r + e % r) * K + (ent & 31);
+        p.part_ml[part * 2] = -INFINITY;
+        p.part_ml[part * 2 + 1] = 0.f;
+      }
+    }
 #pragma unroll 1
     for (int ch = warp; ch * tpc < n; ch += 4) {
       const int ncol = min(tpc, n - ch * tpc) * r;  // real columns of this tile

@@ -98,3 +98,22 @@ def test_prefill_indexer_bad_seq_len_flags_and_fills():
     assert st != 0 and flags & 2
     assert np.isneginf(got[32:]).all()
     check_pooled(got[:32], ref[:32])
+
+
+def test_prefill_bad_block_flags_and_leaves_it_out():
+    # a block-table entry outside the pool in a prefill chunk: the status word
+    # says so, and the attend leaves the block out (finite outputs, no stale partials)
+    from _helpers import gpu_path
+    w = ms.make_workload("fp8_prefill", seed=85, seq_lens=(1500,), q_per_seq=40)
+    c = ms.make_case(w, device="cuda")
+    c["block_table"][0, 3] = c["num_blocks"] + 9
+    cache, batch, iq, q = bind(c)
+    cfg = msa.default_config(w.topk)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    rows = w.num_seqs * w.q_per_seq
+    topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device="cuda")
+    out = torch.full((rows, w.num_q_heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, None, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    assert st != 0 and flags & 1
+    assert torch.isfinite(out.float()).all()
