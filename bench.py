@@ -35,9 +35,13 @@ WORKLOAD_TEXT = {
                    "per-query top-16, causal",
 }
 
-def kernels_per_step(q_per_seq: int) -> int:
-    """Launches of one msa_decode: indexer, top-k, attend (each new token its own
-    one-token sequence in the attend, whatever the count)."""
+def kernels_per_step(w) -> int:
+    """Launches of one msa_decode: indexer, top-k, attend; a prefill chunk (more
+    than 8 new tokens) over an FP8 cache with 1, 2, 4 or 8 q heads a group runs
+    the key-block-major attend instead: count, scan, fill, attend, combine."""
+    r = w.num_q_heads // w.num_kv_heads
+    if w.q_per_seq > 8 and w.kv_dtype == "fp8" and r in (1, 2, 4, 8):
+        return 7
     return 3
 
 
@@ -453,7 +457,7 @@ def main():
                           "peak_kind": peak_kind + " (bf16 burst x 2 for e4m3, the nominal ratio)"}),
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": kernels_per_step(w.q_per_seq) * args.steps,
+            "gpu_launches": kernels_per_step(w) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -330,7 +330,7 @@ struct FragJob {
 
 msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, const float* pooled, int32_t* topk_idx,
                       float* topk_score, void* ws, const Plan* pl, cudaStream_t st, bool pdl, bool clear_ctr,
-                      const FragJob* frag_job = nullptr) {
+                      const FragJob* frag_job = nullptr, bool warp_rows = false) {
   TopkParams tp;
   // positions T - Q + i are the same with or without virtual sequences: the real batch
   Plan real;
@@ -351,6 +351,9 @@ msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, cons
   tp.frag = nullptr;
   tp.colf = nullptr;
   if (frag_job && pl) set_frag_job(tp, frag_job->c, cfg, frag_job->q, frag_job->hq, *pl, ws);
+  // one warp per row: for many short rows with nothing else to do (no scores,
+  // fragments or counters)
+  if (warp_rows && !topk_score && !tp.frag && !tp.zero) return cuda_status(launch_topk_warp(tp, st, pdl));
   return cuda_status(launch_topk(tp, st, pdl));
 }
 
@@ -563,8 +566,8 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, cons
   float* pooled = at<float>(workspace, pl.off_pooled);
   if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st)) != MSA_OK) return s;
   if (pl.k2q) {
-    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, false)) !=
-        MSA_OK)
+    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, false,
+                      nullptr, true)) != MSA_OK)
       return s;
     return run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st);
   }

@@ -192,6 +192,8 @@ cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexer
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
                            bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);
+// one warp per row (K <= 32; no scores, no fragment or counter job)
+cudaError_t launch_topk_warp(const TopkParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attend(int fmt, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, const AttendParams& p,
                           int num_sms, cudaStream_t st, bool pdl);

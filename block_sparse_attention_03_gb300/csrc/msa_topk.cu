@@ -345,6 +345,186 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
   pdl_launch_dependents();
 }
 
+// The top-k blocks of one (query, group) row for the query at position pos,
+// selected by one warp with the rule of the top-k kernel (vLLM Day-0 blog,
+// "MSA 入门"): forced init / local / own blocks, then the highest pooled scores
+// among the other visible blocks, ties to the smaller id, ascending.  Returns
+// in lane k (k < the count) the k-th block id, -1 in the other lanes.
+// Candidates are read interleaved (lane + 32 i: coalesced, and in id order
+// when taken row by row).  Fast path: T = the kfree-th largest lane maximum
+// bounds the wanted scores from below; the candidates >= T (at most 64) are
+// ranked.  Otherwise an exact 4 x 8-bit radix select.
+// scratch: sk[64], si[64], hist[256], out[32] in shared memory.
+__device__ __noinline__ int warp_select_row(const float* __restrict__ pr, int pos, int K, int init_blocks,
+                                            int local_blocks, uint32_t* sk, int* si, int* hist, int* out, int lane) {
+  const unsigned FULL = 0xffffffffu;
+  const unsigned lt = (1u << lane) - 1u;
+  const int recent = pos / kBlock;
+  const int n_init = min(init_blocks, recent);
+  const int n_local = min(local_blocks, recent - n_init);
+  const int lo = n_init, hi = recent - n_local;
+  const int ncand = hi - lo;
+  const int kfree = K - n_init - n_local - 1;
+  const int per = (ncand + 31) / 32;
+  int n_sel = 0;
+  if (ncand <= kfree) {
+    for (int c = lane; c < ncand; c += 32) out[n_init + c] = lo + c;
+    n_sel = ncand;
+  } else if (kfree > 0) {
+    n_sel = kfree;
+    // lane maxima, then the kfree-th largest of them (ties by lane)
+    uint32_t m = 0;
+#pragma unroll 4
+    for (int i = 0; i < per; ++i) {
+      const int c = lane + 32 * i;
+      if (c < ncand) m = max(m, float_order_key(pr[lo + c]));
+    }
+    int rank = 0;
+#pragma unroll 8
+    for (int x = 0; x < 32; ++x) {
+      const uint32_t o = __shfl_sync(FULL, m, x);
+      rank += (o > m) || (o == m && x < lane);
+    }
+    const unsigned who = __ballot_sync(FULL, rank == kfree - 1);
+    const uint32_t T = __shfl_sync(FULL, m, __ffs(who) - 1);
+    // candidates >= T, compacted in id order
+    int C = 0;
+    for (int i = 0; i < per; ++i) {
+      const int c = lane + 32 * i;
+      const uint32_t key = (c < ncand) ? float_order_key(pr[lo + c]) : 0u;
+      const bool in = c < ncand && key >= T;
+      const unsigned bal = __ballot_sync(FULL, in);
+      const int at = C + __popc(bal & lt);
+      if (in && at < 64) {
+        sk[at] = key;
+        si[at] = lo + c;
+      }
+      C += __popc(bal);
+    }
+    __syncwarp();
+    if (C <= 64) {
+      // kept iff fewer than kfree of them beat it (higher key, or equal key and smaller id)
+      bool sel[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = lane + 32 * h;
+        sel[h] = false;
+        if (e < C) {
+          const uint32_t ke = sk[e];
+          int beat = 0;
+          for (int x = 0; x < C; ++x) {
+            const uint32_t kx = sk[x];
+            beat += (kx > ke) || (kx == ke && x < e);
+          }
+          sel[h] = beat < kfree;
+        }
+      }
+      const unsigned b0 = __ballot_sync(FULL, sel[0]), b1 = __ballot_sync(FULL, sel[1]);
+      if (sel[0]) out[n_init + __popc(b0 & lt)] = si[lane];
+      if (sel[1]) out[n_init + __popc(b0) + __popc(b1 & lt)] = si[lane + 32];
+    } else {
+      // exact radix select of the kfree-th key (heavy ties), then one pass in id order
+      uint32_t prefix = 0, pmask = 0;
+      int remaining = kfree;
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int k = lane; k < 256; k += 32) hist[k] = 0;
+        __syncwarp();
+        for (int i = 0; i < per; ++i) {
+          const int c = lane + 32 * i;
+          if (c < ncand) {
+            const uint32_t key = float_order_key(pr[lo + c]);
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+          }
+        }
+        __syncwarp();
+        // lane l owns digits [8l, 8l+8); suffix sums from the top digit down
+        int own = 0;
+        for (int k = 0; k < 8; ++k) own += hist[8 * lane + k];
+        int suf = own;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(FULL, suf, o);
+          if (lane + o < 32) suf += y;
+        }
+        const int above = suf - own;
+        int digit = -1, need = 0;
+        if (above < remaining && suf >= remaining) {
+          int acc = above;
+          for (int k = 7; k >= 0; --k) {
+            const int hk = hist[8 * lane + k];
+            if (acc + hk >= remaining) {
+              digit = 8 * lane + k;
+              need = remaining - acc;
+              break;
+            }
+            acc += hk;
+          }
+        }
+        const unsigned src = __ballot_sync(FULL, digit >= 0);
+        const int sl = __ffs(src) - 1;
+        digit = __shfl_sync(FULL, digit, sl);
+        remaining = __shfl_sync(FULL, need, sl);
+        prefix |= (uint32_t)digit << shift;
+        pmask |= 255u << shift;
+        __syncwarp();
+      }
+      int base_eq = 0, base_sel = 0;
+      for (int i = 0; i < per; ++i) {
+        const int c = lane + 32 * i;
+        const uint32_t key = (c < ncand) ? float_order_key(pr[lo + c]) : 0u;
+        const bool eq = c < ncand && key == prefix;
+        const unsigned beq = __ballot_sync(FULL, eq);
+        const bool take = (c < ncand && key > prefix) || (eq && base_eq + __popc(beq & lt) < remaining);
+        const unsigned btk = __ballot_sync(FULL, take);
+        const int at = n_init + base_sel + __popc(btk & lt);
+        if (take && at < K) out[at] = lo + c;
+        base_eq += __popc(beq);
+        base_sel += __popc(btk);
+      }
+    }
+  }
+  // forced blocks: [0, n_init) first, [hi, recent] last
+  for (int k = lane; k < n_init; k += 32) out[k] = k;
+  const int tail = n_init + n_sel;
+  for (int k = tail + lane; k < K; k += 32) {
+    const int b = hi + (k - tail);
+    out[k] = (b <= recent) ? b : -1;
+  }
+  __syncwarp();
+  const int id = (lane < K) ? out[lane] : -1;
+  __syncwarp();
+  return id;
+}
+
+// One warp per (token, group) row, 8 rows a CTA: for the many short rows of a
+// prefill chunk, where a CTA per row spends its time in block-wide syncs.
+// Same rule and output as topk_kernel (no scores, no fragment or counter job).
+constexpr int kTopkWarpRows = 8;
+__global__ void __launch_bounds__(32 * kTopkWarpRows) topk_warp_kernel(const TopkParams p) {
+  __shared__ uint32_t sk[kTopkWarpRows][64];
+  __shared__ int si[kTopkWarpRows][64];
+  __shared__ int hist[kTopkWarpRows][256];
+  __shared__ int outb[kTopkWarpRows][32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BatchDev bt = p.batch;
+  const long rows = (long)bt.S * bt.Q * p.G;
+  const long row = (long)blockIdx.x * kTopkWarpRows + warp;
+  if (row >= rows) return;
+  const int sq = (int)(row / p.G);
+  const int s = sq / bt.Q, i = sq % bt.Q;
+  const int T = bt.seq_len(s);
+  int id = -1;
+  if (T < bt.Q || T > bt.max_nb * kBlock) {
+    if (lane == 0 && i == 0 && row % p.G == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
+  } else {
+    id = warp_select_row(p.pooled + (size_t)row * bt.max_nb, T - bt.Q + i, p.topk, p.init_blocks, p.local_blocks,
+                         sk[warp], si[warp], hist[warp], outb[warp], lane);
+  }
+  if (lane < p.topk) p.topk_idx[(size_t)row * p.topk + lane] = id;
+}
+
 // Union of the Q queries' selections of one (sequence, group), ascending, with
 // a bit mask of the queries that chose each block.
 __global__ void __launch_bounds__(256) union_kernel(const UnionParams p) {
@@ -439,6 +619,14 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(threads), 0, st, pdl, attr);
   if (wide) return cudaLaunchKernelEx(&cfg, topk_kernel<1024>, p);
   return cudaLaunchKernelEx(&cfg, topk_kernel<kTopkThreads>, p);
+}
+
+cudaError_t launch_topk_warp(const TopkParams& p, cudaStream_t st, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  const long rows = (long)p.batch.S * p.batch.Q * p.G;
+  const long grid = (rows + kTopkWarpRows - 1) / kTopkWarpRows;
+  cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)(grid > 0 ? grid : 1)), dim3(32 * kTopkWarpRows), 0, st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, topk_warp_kernel, p);
 }
 
 cudaError_t launch_union(const UnionParams& p, cudaStream_t st, bool pdl) {

@@ -117,3 +117,28 @@ def test_prefill_bad_block_flags_and_leaves_it_out():
     st, flags = msa.msa_read_device_status(ws)
     assert st != 0 and flags & 1
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("zero_idx,init,local", [(False, 0, 0), (True, 0, 0), (False, 2, 3)])
+def test_prefill_warp_topk_equals_block_topk(zero_idx, init, local):
+    # msa_decode of a prefill chunk selects with one warp per row; the staged
+    # msa_topk_blocks (one CTA per row, checked against the oracle in
+    # test_topk_gpu.py) must give the same rows on the same pooled scores,
+    # ties included (a zero index cache ties every block)
+    w = ms.make_workload("fp8_prefill", seed=86, seq_lens=(128 * 40 + 5, 3000), q_per_seq=48)
+    c = ms.make_case(w, device="cuda")
+    if zero_idx:
+        c["idx"].zero_()
+    cfg = msa.Config(topk=16, init_blocks=init, local_blocks=local)
+    cache, batch, iq, q = bind(c)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    rows, G = w.num_seqs * w.q_per_seq, w.num_kv_heads
+    topk = torch.full((rows, G, 16), -7, dtype=torch.int32, device="cuda")
+    out = torch.empty((rows, w.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, None, ws)
+    pooled = torch.empty((rows, G, w.max_blocks), dtype=torch.float32, device="cuda")
+    msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws)
+    ref = torch.full_like(topk, -9)
+    msa.msa_topk_blocks(batch, cfg, G, pooled, ref, None, ws)
+    assert msa.msa_read_device_status(ws)[0] == 0
+    assert torch.equal(topk, ref)
