@@ -142,3 +142,25 @@ def test_prefill_warp_topk_equals_block_topk(zero_idx, init, local):
     msa.msa_topk_blocks(batch, cfg, G, pooled, ref, None, ws)
     assert msa.msa_read_device_status(ws)[0] == 0
     assert torch.equal(topk, ref)
+
+
+@pytest.mark.parametrize("over,cfg", [
+    (dict(seq_lens=(1800,), q_per_seq=24, num_q_heads=4), None),           # 1 q head a group: 8 tokens a tile
+    (dict(seq_lens=(2500, 1300), q_per_seq=16, topk=32), None),             # 32 slots a token
+    (dict(seq_lens=(3000,), q_per_seq=20), dict(init_blocks=1, local_blocks=2)),
+])
+def test_prefill_key_block_major_variants(over, cfg):
+    from _helpers import check_out, check_selection, gpu_path
+    w = ms.make_workload("fp8_prefill", seed=87, **over)
+    c = ms.make_case(w, device="cuda")
+    conf = msa.Config(topk=w.topk, **(cfg or {}))
+    g = gpu_path(c, cfg=conf)
+    h = ms.case_to_host(c)
+    ref = _oracle(c, w)
+    init, local = (cfg or {}).get("init_blocks", 0), (cfg or {}).get("local_blocks", 0)
+    check_selection(g["topk"], ref, w.seq_lens, w.q_per_seq, w.topk, init, local)
+    out = np.zeros_like(g["out"])
+    for s in range(w.num_seqs):
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+    check_out(g["out"], out)
