@@ -366,32 +366,52 @@ def main():
     }
     clocks = sampler.stop()
 
-    # ---------------- end to end through the public API with host buffers
-    h_iq = torch.empty_like(case["index_q"], device="cpu").pin_memory()
-    h_q = torch.empty_like(case["q"], device="cpu").pin_memory()
-    h_iq.copy_(case["index_q"].cpu())
-    h_q.copy_(case["q"].cpu())
-    h_lens = case["seq_lens"].cpu().pin_memory()
-    h_bt = case["block_table"].cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_topk = torch.empty(topk.shape, dtype=topk.dtype).pin_memory()
+    # ---------------- end to end through the public API with host buffers.  A
+    # step's inputs (index queries, queries, sequence lengths, block table) travel
+    # in one pinned host buffer and one copy, its results (output, selection) in
+    # one device buffer and one copy back, as a serving loop packs them; the
+    # library reads and writes views of those device buffers.
+    def packed(tensors):
+        offs, o = [], 0
+        for t in tensors:
+            offs.append(o)
+            o += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, o
+
+    def view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    ins = [case["index_q"], case["q"], case["seq_lens"], case["block_table"]]
+    in_offs, in_bytes = packed(ins)
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    for t, o in zip(ins, in_offs):
+        view(h_in, o, t).copy_(t.cpu())
+    e_iq, e_q, e_lens, e_bt = (view(d_in, o, t) for t, o in zip(ins, in_offs))
+    e_batch = msa.Batch(e_lens, e_bt, w.q_per_seq)
+    e_iqq = msa.Query(e_iq, w.q_dtype, case["index_q_scale"])
+    e_qq = msa.Query(e_q, w.q_dtype, case["q_scale"])
+    res = [out, topk]
+    res_offs, res_bytes = packed(res)
+    d_res = torch.empty(res_bytes, dtype=torch.uint8, device=dev)
+    h_res = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
+    e_out, e_topk = (view(d_res, o, t) for t, o in zip(res, res_offs))
     e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush()
         e2e_evs[i][0].record(stream)
-        case["index_q"].copy_(h_iq, non_blocking=True)
-        case["q"].copy_(h_q, non_blocking=True)
-        case["seq_lens"].copy_(h_lens, non_blocking=True)
-        case["block_table"].copy_(h_bt, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-        h_topk.copy_(topk, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        msa.msa_decode(cache, e_batch, cfg, e_iqq, e_qq, w.num_q_heads, e_topk, e_out, None, ws, stream)
+        h_res.copy_(d_res, non_blocking=True)
         e2e_evs[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in (h_iq, h_q, h_lens, h_bt))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_topk))
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in res)
+    if not torch.equal(view(h_res, res_offs[1], topk), topk.cpu()):
+        raise RuntimeError("the end-to-end selection differs from the device-timed one")
     st, flags = msa.msa_read_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {msa.msa_status_string(st)} flags {flags}")
