@@ -1,6 +1,7 @@
 // Key-block-major attend of prefill chunks: the selection inverted into lists
-// (the model page's key -> query CSR, `build_k2q_csr`) and the per-token merge
-// of the per-block partials.
+// (the key -> query CSR `build_k2q_csr` of the vLLM MiniMax-M3 model page,
+// "vllm.models.minimax_m3.nvidia.model") and the per-token merge of the
+// per-block partials.
 //
 // Count: for every (token, group, slot) whose selected block is b, one more
 // entry in list (sequence, group, b).  Scan (one CTA): each list's first entry
@@ -8,9 +9,8 @@
 // (token * 32 + slot) into its list, in arrival order (the per-entry results
 // do not depend on it).  The attend (msa_attend.cu) reads each item's K/V tile
 // once and writes one partial (o, m, l) per (token, head, slot); combine
-// merges a token's slots by log-sum-exp (MiniMax Sparse Attention model page,
-// "Top-k block selection": exact softmax over the union of the token's
-// selected blocks).
+// merges a token's slots by log-sum-exp: the exact softmax over all of the
+// token's selected blocks (vLLM Day-0 blog, section "MSA 入门").
 #include "msa_device.cuh"
 #include "msa_internal.h"
 

@@ -1,9 +1,10 @@
 // Indexer score + block max-pool for prefill chunks on the 5th-generation
 // tensor cores (tcgen05, accumulators in tensor memory).
 //
-// What it computes is the indexer of the decode path (MiniMax Sparse Attention
-// model page, "Lightning indexer" / "Top-k block selection"; vLLM Day-0 blog,
-// the MSA indexer prefill kernel): for query token i of sequence s and group g,
+// What it computes is the indexer of the decode path (vLLM Day-0 blog, section
+// "MSA 入门"; section "NVIDIA Blackwell 优化的 MSA 内核" names an MSA indexer
+// prefill kernel):
+// for query token i of sequence s and group g,
 //   P[s, i, g, b] = col_const * max over keys t of block b with t <= pos(i) of
 //                   (index_q[s, i, g] . ik[t]) * kscale[t],
 // -inf where block b holds no visible key.  With thousands of new tokens the

@@ -1,8 +1,8 @@
 """The indexer of prefill chunks (more than 8 new tokens per sequence, FP8
 index cache), which runs on the tcgen05 tensor cores with the query tokens
-as the MMA's M side, against the oracle's pooled scores (MiniMax Sparse
-Attention model page, "Lightning indexer"; vLLM Day-0 blog, MSA indexer
-prefill).  The cases cover one and several 128-row query tiles, ragged last
+as the MMA's M side, against the oracle's pooled scores (vLLM Day-0 blog,
+sections "MSA 入门" and "NVIDIA Blackwell 优化的 MSA 内核", which names an MSA indexer prefill
+kernel).  The cases cover one and several 128-row query tiles, ragged last
 tiles, several sequences of different lengths, e4m3 index queries (one MMA
 term instead of the bf16 hi + lo pair), 1 / 2 / 4 / 8 groups (128, 64, 32, 16
 tokens a tile) and a bad block-table entry.

@@ -1,6 +1,6 @@
 """Block selection alone: msa_topk_blocks on given pooled scores against the
-oracle's selection rule (MiniMax Sparse Attention model page, "Top-k block
-selection"; vLLM Day-0 blog, section on the MSA indexer).
+oracle's selection rule (vLLM Day-0 blog, section "MSA 入门"; the model
+page's top-k buffer, `MiniMaxM3Model`).
 
 Both sides see the same fp32 scores, so the selections must be identical,
 ties included (equal scores keep the smaller block id).  The cases reach
