@@ -220,7 +220,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
     pl.off_kcur = o; o = align256(o + L * 4);
     pl.off_kitem = o; o = align256(o + (L + 1) * 4);
     pl.off_kent = o; o = align256(o + E * 4);
-    pl.off_kpo = o; o = align256(o + P * 128 * 4);
+    pl.off_kpo = o; o = align256(o + P * 128 * 2);
     pl.off_kpml = o; o = align256(o + P * 2 * 4);
   }
   pl.total = o;
@@ -461,7 +461,7 @@ msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_confi
   kp.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
   kp.q_scale = kp.q_fp8 ? q->scale : 1.f;
   kp.col_const = cfg->sm_scale * 1.4426950408889634f;
-  kp.part_o = at<float>(ws, pl.off_kpo);
+  kp.part_o = at<uint16_t>(ws, pl.off_kpo);
   kp.part_ml = at<float>(ws, pl.off_kpml);
   kp.out = out;
   kp.lse = lse;

@@ -1260,6 +1260,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
         for (int mm = 0; mm < 8; ++mm)
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) os[col * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
+        if (g8 == 0) os[col * kMergeRow + 128] = lsum;  // the row's padding holds its l
         if (g8 == 0 && col < ncol) {
           const int ent = hdr[4 + ch * tpc + col / r];
           const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
@@ -1271,14 +1272,20 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       for (int col = 0; col < ncol; ++col) {
         const int ent = hdr[4 + ch * tpc + col / r];
         const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
+        // o / l in fp16 (|o / l| <= max |v|): half the bytes of the fp32 partial
+        const float lc = os[col * kMergeRow + 128];
+        const float inv = lc > 0.f ? __fdividef(1.f, lc) : 0.f;
         float v4[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {  // dim d = 4 lane + t from its accumulator row
           const int d = 4 * lane + t, q = d >> 4, rem = d & 15;
           const int gg = ((q & 3) << 1) | (q >> 2);
-          v4[t] = os[col * kMergeRow + 16 * (rem >> 1) + 8 * (rem & 1) + gg];
+          v4[t] = os[col * kMergeRow + 16 * (rem >> 1) + 8 * (rem & 1) + gg] * inv;
         }
-        reinterpret_cast<float4*>(p.part_o + part * 128)[lane] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+        uint2 pk;
+        pk.x = pack_f16x2(v4[0], v4[1]);
+        pk.y = pack_f16x2(v4[2], v4[3]);
+        reinterpret_cast<uint2*>(p.part_o + part * 128)[lane] = pk;
       }
       __syncwarp();
     }

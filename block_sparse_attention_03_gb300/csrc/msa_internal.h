@@ -175,7 +175,7 @@ struct K2qParams {
   const void* q;             // [S*Q][G*r][128]
   int32_t q_fp8;
   float q_scale, col_const;
-  float* part_o;             // [S*Q*G*r*topk][128] per (token, head, slot)
+  uint16_t* part_o;          // [S*Q*G*r*topk][128] fp16 o / l of each (token, head, slot)
   float* part_ml;            // [S*Q*G*r*topk][2]
   void* out;                 // bf16 [S*Q][G*r][128]
   float* lse;

@@ -105,14 +105,17 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
       const long part = row * p.topk + k;
       const float m = __ldcg(p.part_ml + part * 2), l = __ldcg(p.part_ml + part * 2 + 1);
       if (m == -INFINITY) continue;
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + part * 128) + lane);
+      // the partial holds o / l (fp16): its weight is l * 2^(m - M)
+      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + part * 128) + lane);
+      const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&pk.x));
+      const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&pk.y));
       const float mn = fmaxf(M, m);
-      const float a = k2q_ex2(M - mn), w = k2q_ex2(m - mn);  // M = -inf: a = 0
-      acc.x = acc.x * a + w * o.x;
-      acc.y = acc.y * a + w * o.y;
-      acc.z = acc.z * a + w * o.z;
-      acc.w = acc.w * a + w * o.w;
-      Lsum = Lsum * a + w * l;
+      const float a = k2q_ex2(M - mn), w = k2q_ex2(m - mn) * l;  // M = -inf: a = 0
+      acc.x = acc.x * a + w * o01.x;
+      acc.y = acc.y * a + w * o01.y;
+      acc.z = acc.z * a + w * o23.x;
+      acc.w = acc.w * a + w * o23.y;
+      Lsum = Lsum * a + w;
       M = mn;
     }
     const float inv = Lsum > 0.f ? __fdividef(1.f, Lsum) : 0.f;

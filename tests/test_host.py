@@ -100,11 +100,11 @@ def test_bad_arguments_rejected_before_launch(lib):
 
 
 def test_prefill_workspace_holds_the_partials(lib):
-    # a prefill chunk over an FP8 cache keeps one fp32 partial (o[128], m, l) per
-    # (token, q head, selected block): 8,192 tokens x 16 heads x 16 -> >= 1.09 GB
+    # a prefill chunk over an FP8 cache keeps one partial (fp16 o / l, fp32 m and l)
+    # per (token, q head, selected block): 8,192 tokens x 16 heads x 16 -> >= 554 MB
     c, b, f = _structs(b__num_seqs=1, b__q_per_seq=8192, b__max_blocks_per_seq=576, c__num_blocks=600)
     n = lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 16)
-    assert n >= 8192 * 16 * 16 * 130 * 4
+    assert n >= 8192 * 16 * 16 * (128 * 2 + 2 * 4)
     # the same chunk over an NVFP4 cache attends per token: no such partials
     c2, b2, f2 = _structs(b__num_seqs=1, b__q_per_seq=8192, b__max_blocks_per_seq=576, c__num_blocks=600,
                           c__kv_dtype=2)
