@@ -164,3 +164,24 @@ def test_prefill_key_block_major_variants(over, cfg):
         o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
         out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
     check_out(g["out"], out)
+
+
+def test_prefill_bf16_cache_per_token_path():
+    # BF16 keys / index keys: the decode indexer over 8-token virtual sequences
+    # and the per-token attend (the key-block-major path is FP8 only)
+    from _helpers import check_out, check_selection, check_pooled, gpu_path
+    w = ms.make_workload("fp8_prefill", seed=88, seq_lens=(2200, 900), q_per_seq=24,
+                         kv_dtype="bf16", index_dtype="bf16")
+    c = ms.make_case(w, device="cuda")
+    h = ms.case_to_host(c)
+    ref = _oracle(c, w)
+    got, st, flags = _pooled(c, w)
+    assert st == 0, (msa.msa_status_string(st), flags)
+    check_pooled(got, ref)
+    g = gpu_path(c)
+    check_selection(g["topk"], ref, w.seq_lens, w.q_per_seq, w.topk)
+    out = np.zeros_like(g["out"])
+    for s in range(w.num_seqs):
+        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+    check_out(g["out"], out)
