@@ -47,16 +47,38 @@ __device__ __forceinline__ void build_qfrag(const void* q, bool q_fp8, const lon
     const long row = rows[nt];
     float vals[KS][2][TPR];
     float amax = 0.f;
+    if (KEYFMT == FMT_FP8 && !q_fp8) {
+      // e4m3 keys, bf16 query: a register's 4 dims are contiguous and 8-byte
+      // aligned (rows start at multiples of 4 elements): one 8-byte load each
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-      for (int rg = 0; rg < 2; ++rg)
+        for (int rg = 0; rg < 2; ++rg) {
+          uint2 w = make_uint2(0u, 0u);
+          if (row >= 0)
+            w = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(q) + (size_t)row +
+                                                frag_dim<KEYFMT>(ks, rg, 0, j));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+          const float f[4] = {a.x, a.y, b.x, b.y};
 #pragma unroll
-        for (int t = 0; t < TPR; ++t) {
-          const float v = (row >= 0) ? q_elem(q, q_fp8, (size_t)row + frag_dim<KEYFMT>(ks, rg, t, j)) : 0.f;
-          vals[ks][rg][t] = v;
-          amax = fmaxf(amax, fabsf(v));
+          for (int t = 0; t < TPR; ++t) {
+            vals[ks][rg][t] = f[t];
+            amax = fmaxf(amax, fabsf(f[t]));
+          }
         }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+          for (int t = 0; t < TPR; ++t) {
+            const float v = (row >= 0) ? q_elem(q, q_fp8, (size_t)row + frag_dim<KEYFMT>(ks, rg, t, j)) : 0.f;
+            vals[ks][rg][t] = v;
+            amax = fmaxf(amax, fabsf(v));
+          }
+    }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     int e = 0;
