@@ -1118,6 +1118,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
   const BatchDev bt = p.batch;
   const int G = p.G, r = p.r, H = G * r, Q = bt.Q, K = p.topk;
   const int tpc = 8 / r;  // tokens per 8-column tile
+  const int lr = __ffs(r) - 1;  // r is 1, 2, 4 or 8: col / r = col >> lr
   const long L = (long)bt.S * G * bt.max_nb;
   const int items = p.item_off[L];
 
@@ -1205,8 +1206,8 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       const int chunks = 128 * esz / 16;       // 16-byte pieces a row
       const int qstride = 128 * esz + 32;      // bytes between staged rows
       for (int e = lane; e < ncol * chunks; e += 32) {
-        const int col = e / chunks, pc = e % chunks;
-        const long row = (long)(hdr[4 + ch * tpc + col / r] >> 5) * H + g * r + col % r;
+        const int col = e >> (p.q_fp8 ? 3 : 4), pc = e & (chunks - 1);  // chunks = 8 or 16
+        const long row = (long)(hdr[4 + ch * tpc + (col >> lr)] >> 5) * H + g * r + (col & (r - 1));
         *reinterpret_cast<uint4*>(qo + (size_t)col * qstride + 16 * pc) =
             *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + (size_t)row * 128 * esz + 16 * pc);
       }
@@ -1230,7 +1231,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
         const int col = 2 * j + c;
         colf[c] = cf[0][c];
         if (col < ncol) {
-          const int token = hdr[4 + ch * tpc + col / r] >> 5;
+          const int token = hdr[4 + ch * tpc + (col >> lr)] >> 5;
           qlim[c] = T - Q + (token - s * Q);
         } else {
           qlim[c] = -1;
@@ -1262,16 +1263,16 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
           for (int h2 = 0; h2 < 2; ++h2) os[col * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
         if (g8 == 0) os[col * kMergeRow + 128] = lsum;  // the row's padding holds its l
         if (g8 == 0 && col < ncol) {
-          const int ent = hdr[4 + ch * tpc + col / r];
-          const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
+          const int ent = hdr[4 + ch * tpc + (col >> lr)];
+          const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
           p.part_ml[part * 2] = m_run[c];
           p.part_ml[part * 2 + 1] = lsum;
         }
       }
       __syncwarp();
       for (int col = 0; col < ncol; ++col) {
-        const int ent = hdr[4 + ch * tpc + col / r];
-        const long part = ((long)(ent >> 5) * H + g * r + col % r) * K + (ent & 31);
+        const int ent = hdr[4 + ch * tpc + (col >> lr)];
+        const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
         // o / l in fp16 (|o / l| <= max |v|): half the bytes of the fp32 partial
         const float lc = os[col * kMergeRow + 128];
         const float inv = lc > 0.f ? __fdividef(1.f, lc) : 0.f;
