@@ -151,7 +151,8 @@ struct Plan {
   // prefill chunks over an FP8 cache: the key-block-major attend (selection lists,
   // one partial per (token, head, slot), a combine pass)
   bool k2q = false;
-  size_t off_kcnt = 0, off_koff = 0, off_kcur = 0, off_kitem = 0, off_kent = 0, off_kpo = 0, off_kpml = 0;
+  size_t off_kcnt = 0, off_koff = 0, off_kcur = 0, off_kitem = 0, off_kent = 0, off_klist = 0, off_kpo = 0,
+         off_kpml = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -220,6 +221,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
     pl.off_kcur = o; o = align256(o + L * 4);
     pl.off_kitem = o; o = align256(o + (L + 1) * 4);
     pl.off_kent = o; o = align256(o + E * 4);
+    pl.off_klist = o; o = align256(o + E * 4);
     pl.off_kpo = o; o = align256(o + P * 128 * 2);
     pl.off_kpml = o; o = align256(o + P * 2 * 4);
   }
@@ -455,6 +457,7 @@ msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_confi
   kp.cur = at<int32_t>(ws, pl.off_kcur);
   kp.item_off = at<int32_t>(ws, pl.off_kitem);
   kp.entries = at<int32_t>(ws, pl.off_kent);
+  kp.item_list = at<int32_t>(ws, pl.off_klist);
   kp.k_scale = c->k_scale;
   kp.v_scale = c->v_scale;
   kp.q = q->data;

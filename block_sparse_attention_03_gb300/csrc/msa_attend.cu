@@ -1133,13 +1133,7 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
 
   // thread 0: item `it` into stage st (header, entries, K/V tile and scales)
   auto issue = [&](int it, int st) {
-    long lo = 0, hi = L;  // the list: largest i with item_off[i] <= it
-    while (hi - lo > 1) {
-      const long mid = (lo + hi) >> 1;
-      if (p.item_off[mid] <= it) lo = mid;
-      else hi = mid;
-    }
-    const long list = lo;
+    const long list = p.item_list[it];
     const int e0 = p.off[list] + (it - p.item_off[list]) * kK2qTokens;
     const int n = min(kK2qTokens, p.off[list] + p.cnt[list] - e0);
     const int s = (int)(list / ((long)G * bt.max_nb)), g = (int)((list / bt.max_nb) % G), b = (int)(list % bt.max_nb);

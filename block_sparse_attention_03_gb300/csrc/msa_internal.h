@@ -170,6 +170,7 @@ struct K2qParams {
   int32_t* cur;              // [L] fill cursors
   int32_t* item_off;         // [L + 1] first attend item of each list; [L] = items in all
   int32_t* entries;          // [S*Q*G*topk] token * 32 + slot, list by list
+  int32_t* item_list;        // [S*Q*G*topk] (at most one item per entry) the list of each attend item
   const float* k_scale;      // FP8 per-token scales
   const float* v_scale;
   const void* q;             // [S*Q][G*r][128]

@@ -56,11 +56,13 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
   int e0 = se[t] - ne, i0 = si[t] - ni;
   for (long i = l0; i < l1; ++i) {
     const int c = p.cnt[i];
+    const int items = (c + kK2qTokens - 1) / kK2qTokens;
     p.off[i] = e0;
     p.cur[i] = e0;
     p.item_off[i] = i0;
+    for (int k = 0; k < items; ++k) p.item_list[i0 + k] = (int)i;  // the attend's item -> list map
     e0 += c;
-    i0 += (c + kK2qTokens - 1) / kK2qTokens;
+    i0 += items;
   }
   if (t == 1023) p.item_off[L] = si[1023];
 }
