@@ -18,15 +18,30 @@ namespace msa {
 
 namespace {
 
+// Selection entry e = (token, group, slot): its list (sequence, group, block),
+// or -1 for an empty slot (-1) or a block the token cannot see (flagged once,
+// by the count pass, like the per-token attend does).  Count and fill agree.
+__device__ __forceinline__ long k2q_list(const K2qParams& p, long e, bool flag) {
+  const BatchDev bt = p.batch;
+  const int b = p.topk_idx[e];
+  if (b < 0) return -1;
+  const long row = e / p.topk;  // token * G + g
+  const long token = row / p.G;
+  const int s = (int)(token / bt.Q), g = (int)(row % p.G), i = (int)(token % bt.Q);
+  const int T = bt.seq_len(s);
+  if (b >= bt.max_nb || T < bt.Q || T > bt.max_nb * kBlock || b > (T - bt.Q + i) / kBlock) {
+    if (flag) raise_flag(p.status, FLAG_BAD_SELECT, b);
+    return -1;
+  }
+  return ((long)s * p.G + g) * bt.max_nb + b;
+}
+
 __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
   const long n = (long)bt.S * bt.Q * p.G * p.topk;
   for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
-    const int b = p.topk_idx[e];
-    if (b < 0 || b >= bt.max_nb) continue;
-    const long row = e / p.topk;  // token * G + g
-    const int s = (int)(row / ((long)bt.Q * p.G)), g = (int)(row % p.G);
-    atomicAdd(&p.cnt[((long)s * p.G + g) * bt.max_nb + b], 1);
+    const long key = k2q_list(p, e, true);
+    if (key >= 0) atomicAdd(&p.cnt[key], 1);
   }
 }
 
@@ -71,13 +86,11 @@ __global__ void __launch_bounds__(256) k2q_fill_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
   const long n = (long)bt.S * bt.Q * p.G * p.topk;
   for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
-    const int b = p.topk_idx[e];
-    if (b < 0 || b >= bt.max_nb) continue;
-    const long row = e / p.topk;
+    const long key = k2q_list(p, e, false);
+    if (key < 0) continue;
+    const long token = e / p.topk / p.G;
     const int slot = (int)(e % p.topk);
-    const long token = row / p.G;
-    const int s = (int)(token / bt.Q), g = (int)(row % p.G);
-    const int at = atomicAdd(&p.cur[((long)s * p.G + g) * bt.max_nb + b], 1);
+    const int at = atomicAdd(&p.cur[key], 1);
     p.entries[at] = (int)(token * 32 + slot);
   }
 }
@@ -100,10 +113,16 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const long token = row / H;
     const int h = (int)(row % H), g = h / p.r;
     const int32_t* sel = p.topk_idx + (token * p.G + g) * p.topk;
+    // the entries the lists hold (k2q_list's rule), no others: the token's
+    // visible blocks of a well-formed sequence
+    const int s = (int)(token / bt.Q), i = (int)(token % bt.Q);
+    const int T = bt.seq_len(s);
+    const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
     float M = -INFINITY, Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < p.topk; ++k) {
-      if (sel[k] < 0) continue;
+      const int b = sel[k];
+      if (b < 0 || b > last) continue;
       const long part = row * p.topk + k;
       const float m = __ldcg(p.part_ml + part * 2), l = __ldcg(p.part_ml + part * 2 + 1);
       if (m == -INFINITY) continue;

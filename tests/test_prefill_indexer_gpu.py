@@ -185,3 +185,25 @@ def test_prefill_bf16_cache_per_token_path():
         o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
         out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
     check_out(g["out"], out)
+
+
+def test_prefill_invisible_selection_flags_and_is_left_out():
+    # a caller's selection naming a block the token cannot see (the staged
+    # msa_sparse_attend): the status word says so and the output stays finite
+    w = ms.make_workload("fp8_prefill", seed=89, seq_lens=(1300,), q_per_seq=24)
+    c = ms.make_case(w, device="cuda")
+    cache, batch, iq, q = bind(c)
+    cfg = msa.default_config(w.topk)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    rows = w.num_seqs * w.q_per_seq
+    topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device="cuda")
+    out = torch.empty((rows, w.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, None, ws)
+    assert msa.msa_read_device_status(ws)[0] == 0
+    bad = topk.clone()
+    bad[0, 0, 1] = (w.seq_lens[0] - 1) // 128  # token 0 sits in an earlier block: this one is invisible to it
+    out2 = torch.full_like(out, float("nan"))
+    msa.msa_sparse_attend(cache, batch, cfg, q, w.num_q_heads, bad, out2, None, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    assert st != 0 and flags & 4
+    assert torch.isfinite(out2.float()).all()
