@@ -118,26 +118,36 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const int s = (int)(token / bt.Q), i = (int)(token % bt.Q);
     const int T = bt.seq_len(s);
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
-    float M = -INFINITY, Lsum = 0.f;
+    // lane k < topk: slot k's (m, l); the row's max M and weights w_k = l_k 2^(m_k - M)
+    // by warp reductions, then every slot's o / l loaded independently
+    float mk = -INFINITY, lk = 0.f;
+    if (lane < p.topk) {
+      const int b = sel[lane];
+      if (b >= 0 && b <= last) {
+        const long part = row * p.topk + lane;
+        mk = __ldcg(p.part_ml + part * 2);
+        lk = __ldcg(p.part_ml + part * 2 + 1);
+      }
+    }
+    float M = mk;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float wk = (mk == -INFINITY) ? 0.f : k2q_ex2(mk - M) * lk;
+    float Lsum = wk;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int k = 0; k < p.topk; ++k) {
-      const int b = sel[k];
-      if (b < 0 || b > last) continue;
-      const long part = row * p.topk + k;
-      const float m = __ldcg(p.part_ml + part * 2), l = __ldcg(p.part_ml + part * 2 + 1);
-      if (m == -INFINITY) continue;
-      // the partial holds o / l (fp16): its weight is l * 2^(m - M)
-      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + part * 128) + lane);
+      const float w = __shfl_sync(0xffffffffu, wk, k);
+      if (w == 0.f) continue;  // warp-uniform
+      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + (row * p.topk + k) * 128) + lane);
       const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&pk.x));
       const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&pk.y));
-      const float mn = fmaxf(M, m);
-      const float a = k2q_ex2(M - mn), w = k2q_ex2(m - mn) * l;  // M = -inf: a = 0
-      acc.x = acc.x * a + w * o01.x;
-      acc.y = acc.y * a + w * o01.y;
-      acc.z = acc.z * a + w * o23.x;
-      acc.w = acc.w * a + w * o23.y;
-      Lsum = Lsum * a + w;
-      M = mn;
+      acc.x += w * o01.x;
+      acc.y += w * o01.y;
+      acc.z += w * o23.x;
+      acc.w += w * o23.y;
     }
     const float inv = Lsum > 0.f ? __fdividef(1.f, Lsum) : 0.f;
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
