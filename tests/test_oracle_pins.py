@@ -315,3 +315,129 @@ def test_multi_token_causal_positions():
         for g in range(w.num_kv_heads):
             assert pos // 128 in r["topk"][i, g]
             assert np.all(np.isneginf(r["pooled"][i, g, pos // 128 + 1:]))
+
+
+# ---------------------------------------------------------------- query and K/V scales, decoded independently
+
+# OCP MX FP4 E2M1 magnitudes by code (bit 3 = sign), written out from the format
+# definition for the independent decodes below
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).float()
+
+
+def _indep_fp8(codes, scale):
+    """fp32 value of e4m3 codes times their per-row fp32 scale, through torch's cast."""
+    return (_torch_e4m3(codes) * torch.from_numpy(np.asarray(scale, np.float32))[..., None]).numpy()
+
+
+def _indep_nvfp4(packed, sf, gscale):
+    """fp32 NVFP4 value: table-decoded nibbles (low nibble first) x torch-decoded
+    e4m3 block scales, then x the per-tensor scale in fp32."""
+    p = np.asarray(packed, np.uint8)
+    nib = np.stack([p & 0xF, p >> 4], axis=-1).reshape(p.shape[:-1] + (2 * p.shape[-1],))
+    vals = np.where(nib & 8, -1.0, 1.0) * _E2M1_MAG[nib & 7]
+    sfv = np.repeat(_torch_e4m3(sf).numpy().astype(np.float64), 16, axis=-1)
+    return (vals * sfv).astype(np.float32) * np.float32(gscale)
+
+
+@pytest.mark.parametrize("scale", [0.0173, 3.25e-3, 1.0])
+def test_fp8_query_values_match_torch_cast_times_scale(scale):
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    got = O.query_values(codes, "fp8", scale)
+    ref = (_torch_e4m3(codes) * torch.tensor(scale, dtype=torch.float32)).double().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_generated_fp8_queries_decode_with_their_own_scales():
+    # q and index_q of an E4M3-query case have different per-tensor scales; each
+    # decodes as torch's cast times its own scale
+    w, c = _small_case(seq_lens=(600,), q_per_seq=2, kv_dtype="nvfp4", index_dtype="nvfp4", q_dtype="fp8")
+    assert c["q_scale"] != c["index_q_scale"] and c["q_scale"] != 1.0
+    for key in ("q", "index_q"):
+        got = O.query_values(c[key], "fp8", c[key + "_scale"])
+        ref = (_torch_e4m3(c[key]) * torch.tensor(c[key + "_scale"], dtype=torch.float32)).double().numpy()
+        assert np.array_equal(got, ref), key
+
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+def test_kv_tiles_decode_with_their_own_scales(kv):
+    # K and V differ in data and in scales; each tile must decode with its own
+    w, c = _small_case(seq_lens=(300, 200), kv_dtype=kv, index_dtype=kv)
+    for phys in range(c["num_blocks"]):
+        for which in ("k", "v"):
+            if kv == "fp8":
+                ref = _indep_fp8(c[which][phys], c[which + "_scale"][phys])
+            else:
+                ref = _indep_nvfp4(c[which][phys], c[which + "_sf"][phys], c[which + "_global"])
+            got = O.dequant_kv_tile(c, which, phys)
+            assert np.array_equal(got.view(np.uint32), ref.astype(np.float32).view(np.uint32)), (which, phys)
+    if kv == "fp8":
+        assert not np.array_equal(c["k_scale"], c["v_scale"])
+    else:
+        assert c["k_global"] != c["v_global"]
+
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+def test_kv_quantize_dequant_round_trip_within_format_bound(kv):
+    # x -> generator's quantizer -> oracle decode lands within the format's
+    # rounding bound of x, for K and V separately (distinct data, distinct scales)
+    gen = torch.Generator().manual_seed(9)
+    k = torch.randn((2, 4, 128, 128), generator=gen) / math.sqrt(128.0)
+    v = 3.0 * torch.randn((2, 4, 128, 128), generator=gen) / math.sqrt(128.0)
+    w = ms.make_workload("tiny_bf16", seq_lens=(256,), kv_dtype=kv, index_dtype=kv)
+    case = {"workload": w}
+    for name, x in (("k", k), ("v", v)):
+        if kv == "fp8":
+            codes, scale = ms.quantize_fp8_rows(x)
+            case[name], case[name + "_scale"] = codes.numpy(), scale.numpy()
+        else:
+            packed, sf, g = ms.quantize_nvfp4(x)
+            case[name], case[name + "_sf"], case[name + "_global"] = packed.numpy(), sf.numpy(), g
+    for name, x in (("k", k), ("v", v)):
+        xs = x.numpy().astype(np.float64)
+        for phys in range(2):
+            d = O.dequant_kv_tile(case, name, phys).astype(np.float64)
+            if kv == "fp8":
+                # E4M3 round to nearest: |err| <= 2^-4 |x| (normal range) or half the
+                # subnormal step 2^-10, in units of the row scale
+                sc = case[name + "_scale"][phys].astype(np.float64)[..., None]
+                bound = np.maximum(np.abs(xs[phys]) * 2.0 ** -4, sc * 2.0 ** -10) * (1 + 1e-6)
+            else:
+                # E2M1 step within a 16-group is at most 2 (between 4 and 6) in units of
+                # scale x global, half of it after rounding; the e4m3 scale itself carries
+                # a relative error up to 2^-4, which moves the group's largest value by
+                # at most 6 x 2^-4 units
+                sfv = np.repeat(O.e4m3_value(case[name + "_sf"][phys]), 16, axis=-1) * case[name + "_global"]
+                bound = sfv * (1.0 + 6 * 2.0 ** -4) * (1 + 1e-6) + 1e-30
+            assert np.all(np.abs(d - xs[phys]) <= bound), (kv, name)
+        # the scales differ between K and V (V is 3x wider), so a swap is visible
+    if kv == "fp8":
+        assert np.median(case["v_scale"]) > 2 * np.median(case["k_scale"])
+    else:
+        assert case["v_global"] > 2 * case["k_global"]
+
+
+def test_full_topk_equals_dense_sdpa_with_fp8_queries_decoded_independently():
+    # top-k >= blocks: equal to dense causal attention; the reference side decodes
+    # q (E4M3 x its scale) and the FP8 K / V tiles (x their own per-token scales)
+    # through torch's float8 cast, not through the oracle's helpers
+    w, c = _small_case(seq_lens=(900,), q_per_seq=3, kv_dtype="fp8", index_dtype="fp8", q_dtype="fp8", topk=8)
+    r = O.run_path(c)
+    Q, T = w.q_per_seq, w.seq_lens[0]
+    nb = (T + 127) // 128
+    phys = [int(c["block_table"][0, b]) for b in range(nb)]
+    K = np.concatenate([_indep_fp8(c["k"][p], c["k_scale"][p]) for p in phys], axis=1)[:, :T]
+    V = np.concatenate([_indep_fp8(c["v"][p], c["v_scale"][p]) for p in phys], axis=1)[:, :T]
+    q = (_torch_e4m3(c["q"]) * torch.tensor(c["q_scale"], dtype=torch.float32)).double()[:Q]
+    qt = q.permute(1, 0, 2)[None]
+    kt = torch.from_numpy(K.astype(np.float64))[None]
+    vt = torch.from_numpy(V.astype(np.float64))[None]
+    pos = torch.arange(T - Q, T)
+    mask = torch.arange(T)[None, :] <= pos[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=mask, scale=w.head_dim ** -0.5, enable_gqa=True)[0].permute(1, 0, 2).numpy()
+    assert np.allclose(r["out"][:Q], ref, rtol=0, atol=1e-12)
