@@ -623,6 +623,8 @@ namespace {
 
 // Device address of msa_noalloc_scratch on the current device, looked up once
 // per device (the host-side symbol is only a stand-in, never a device address).
+// The cached address assumes the device's context lives as long as the
+// process: a device reset (cudaDeviceReset) is not supported afterwards.
 msa_status_t noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[64];
@@ -663,11 +665,20 @@ extern "C" msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_b
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MSA_ERR_CUDA;
   float* pooled = at<float>(ws, pl.off_pooled);
   if ((s = run_indexer(cache, batch, cfg, index_q, pl, ws, pooled, st)) != MSA_OK) return s;
-  const FragJob fj = {cache, q, num_q_heads};
-  if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, true,
-                    pl.direct ? &fj : nullptr)) != MSA_OK)
-    return s;
-  if ((s = run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st, true)) != MSA_OK) return s;
+  if (pl.k2q) {
+    // a prefill chunk over an FP8 cache: the same chain as msa_decode's
+    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, false,
+                      nullptr, true)) != MSA_OK)
+      return s;
+    if ((s = run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st)) != MSA_OK) return s;
+  } else {
+    const FragJob fj = {cache, q, num_q_heads};
+    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, true,
+                      pl.direct ? &fj : nullptr)) != MSA_OK)
+      return s;
+    if ((s = run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st, true)) != MSA_OK)
+      return s;
+  }
   if (status_out &&
       cudaMemcpyAsync(status_out, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return MSA_ERR_CUDA;

@@ -23,9 +23,11 @@
 // dedicated shared-memory area (named barriers among the consumers only), so
 // the next item's copies keep streaming meanwhile.  A (sequence, group) that
 // fits one split writes its bf16 output and LSE directly; otherwise each split
-// writes a partial and combine_kernel merges them by log-sum-exp (one warp per
-// output row and head).  Every wait is bounded; a wait that gives up raises
-// the timeout flag and the CTA winds down without further copies.
+// writes a partial (o, m, l), and the CTA whose split finishes that
+// (sequence, group) last (an acquire-release atomic count) merges all of its
+// partials by log-sum-exp (merge_splits).  Every wait is bounded; a wait that
+// gives up raises the timeout flag and the CTA winds down without further
+// copies.
 //
 // Tensor-core mapping, keys as MMA rows (the query side is only Q x r <= 32
 // columns wide):

@@ -19,8 +19,10 @@ namespace msa {
 namespace {
 
 // Selection entry e = (token, group, slot): its list (sequence, group, block),
-// or -1 for an empty slot (-1) or a block the token cannot see (flagged once,
-// by the count pass, like the per-token attend does).  Count and fill agree.
+// or -1 for an empty slot (-1), a block the token cannot see, or a block an
+// earlier slot of the same row already names (the last two flagged once, by
+// the count pass; the softmax runs over the selected key set, each key once).
+// Count, fill and combine agree.
 __device__ __forceinline__ long k2q_list(const K2qParams& p, long e, bool flag) {
   const BatchDev bt = p.batch;
   const int b = p.topk_idx[e];
@@ -29,7 +31,10 @@ __device__ __forceinline__ long k2q_list(const K2qParams& p, long e, bool flag) 
   const long token = row / p.G;
   const int s = (int)(token / bt.Q), g = (int)(row % p.G), i = (int)(token % bt.Q);
   const int T = bt.seq_len(s);
-  if (b >= bt.max_nb || T < bt.Q || T > bt.max_nb * kBlock || b > (T - bt.Q + i) / kBlock) {
+  bool bad = b >= bt.max_nb || T < bt.Q || T > bt.max_nb * kBlock || b > (T - bt.Q + i) / kBlock;
+  const int slot = (int)(e - row * p.topk);
+  for (int k = 0; k < slot && !bad; ++k) bad = p.topk_idx[row * p.topk + k] == b;
+  if (bad) {
     if (flag) raise_flag(p.status, FLAG_BAD_SELECT, b);
     return -1;
   }
@@ -121,9 +126,12 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     // lane k < topk: slot k's (m, l); the row's max M and weights w_k = l_k 2^(m_k - M)
     // by warp reductions, then every slot's o / l loaded independently
     float mk = -INFINITY, lk = 0.f;
+    const int bl = lane < p.topk ? sel[lane] : -1;
+    // a block an earlier slot already names has no list entry (k2q_list)
+    const unsigned same = __match_any_sync(0xffffffffu, bl);
     if (lane < p.topk) {
-      const int b = sel[lane];
-      if (b >= 0 && b <= last) {
+      const int b = bl;
+      if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
         const long part = row * p.topk + lane;
         mk = __ldcg(p.part_ml + part * 2);
         lk = __ldcg(p.part_ml + part * 2 + 1);

@@ -573,6 +573,13 @@ __global__ void __launch_bounds__(256) union_kernel(const UnionParams p) {
     int f = b >= 0;
     for (int e2 = 0; e2 < e && f; ++e2) f = ids[e2] != b;
     first[e] = f;
+    // the same block twice in one token's row: attended once, flagged
+    if (b >= 0 && !f) {
+      const int row0 = e - e % p.topk;
+      bool twice = false;
+      for (int e2 = row0; e2 < e && !twice; ++e2) twice = ids[e2] == b;
+      if (twice) raise_flag(p.status, FLAG_BAD_SELECT, b);
+    }
   }
   __syncthreads();
   // position of each unique block = number of unique blocks with a smaller id

@@ -165,6 +165,10 @@ msa_status_t msa_indexer_score(const msa_cache_t* cache, const msa_batch_t* batc
                                msa_stream_t stream);
 
 /* Top-k block selection (step 3) from pooled scores laid out as above.
+ * The output keeps the token-major layout of the model's shared top-k buffer
+ * (API page "vllm.models.minimax_m3.nvidia.model", MiniMaxM3Model: the
+ * indexer writes [tokens, index heads, topk] int32 block ids that the attend
+ * reads back).
  * topk_idx:   int32 [num_seqs * q_per_seq][num_groups][topk], the query's own
  *             block ⌊pos/128⌋ always included (forced, together with the
  *             init/local blocks), the remaining slots filled with the highest
@@ -184,7 +188,10 @@ msa_status_t msa_topk_blocks(const msa_batch_t* batch, const msa_config_t* cfg,
  * out: bf16 [num_seqs * q_per_seq][num_q_heads][head_dim] (caller-allocated).
  * lse: optional fp32 [num_seqs * q_per_seq][num_q_heads], natural-log
  *      log-sum-exp of the scaled logits; may be NULL.
- * A row whose selection holds no visible key gets out = 0, lse = -inf. */
+ * A row whose selection holds no visible key gets out = 0, lse = -inf.
+ * Entries naming a block the query cannot see, or repeating a block an
+ * earlier entry of the same row names, are left out and raise the device
+ * fault flag: the softmax runs over the selected key set, each key once. */
 msa_status_t msa_sparse_attend(const msa_cache_t* cache, const msa_batch_t* batch,
                                const msa_config_t* cfg, const msa_query_t* q,
                                int32_t num_q_heads, const int32_t* topk_idx, void* out,
@@ -231,6 +238,8 @@ msa_status_t msa_dequant_debug(const msa_cache_t* cache, int32_t which,
  *     MSA_ERR_WORKSPACE_TOO_SMALL before any launch.
  *   - The first call on each device looks up the scratch's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     The address is kept for the life of the process: resetting the device
+ *     (cudaDeviceReset) and calling again is not supported.
  *   - Every call shares the one scratch array, which keeps the last call's
  *     contents; each call clears what must start at zero.  Calls that overlap
  *     on the GPU (other streams, other host threads) race on it: serialise them.

@@ -160,10 +160,51 @@ def test_prefill_key_block_major_variants(over, cfg):
     init, local = (cfg or {}).get("init_blocks", 0), (cfg or {}).get("local_blocks", 0)
     check_selection(g["topk"], ref, w.seq_lens, w.q_per_seq, w.topk, init, local)
     out = np.zeros_like(g["out"])
+    lse = np.zeros_like(g["lse"])
     for s in range(w.num_seqs):
-        o, _ = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
+        o, l = O.attend_rows(h, s, g["topk"], w.head_dim ** -0.5)
         out[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+        lse[s * w.q_per_seq:(s + 1) * w.q_per_seq] = l
     check_out(g["out"], out)
+    # the combine's log-sum-exp of the token's slots
+    assert np.abs(g["lse"] - lse).max() < 1e-3
+
+
+@pytest.mark.parametrize("name,over", [
+    ("fp8_prefill", dict(seq_lens=(1700,), q_per_seq=24)),   # key-block-major lists
+    ("fp8_decode", dict(seq_lens=(2600, 1900))),              # per-token union
+])
+def test_repeated_selected_block_attended_once_and_flagged(name, over):
+    # a caller's selection naming one block twice in a row: the softmax runs over
+    # the selected key set with each key once, and the status word says so
+    from _helpers import check_out, gpu_path
+    w = ms.make_workload(name, seed=90, **over)
+    c = ms.make_case(w, device="cuda")
+    g = gpu_path(c)
+    h = ms.case_to_host(c)
+    cache, batch, iq, q = bind(c)
+    cfg = msa.default_config(w.topk)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    bad = g["topk"].copy()
+    rows = w.num_seqs * w.q_per_seq
+    for r in range(0, rows, 3):
+        bad[r, r % w.num_kv_heads, 1] = bad[r, r % w.num_kv_heads, 3]  # slot 1 repeats slot 3
+    out = torch.full((rows, w.num_q_heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((rows, w.num_q_heads), dtype=torch.float32, device="cuda")
+    msa.msa_sparse_attend(cache, batch, cfg, q, w.num_q_heads, torch.from_numpy(bad).cuda(), out, lse, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    assert st != 0 and flags & 4
+    dedup = bad.copy()
+    for r in range(0, rows, 3):
+        dedup[r, r % w.num_kv_heads, 1] = -1
+    ref = np.zeros((rows, w.num_q_heads, 128))
+    ref_lse = np.zeros((rows, w.num_q_heads))
+    for s in range(w.num_seqs):
+        o, l = O.attend_rows(h, s, dedup, w.head_dim ** -0.5)
+        ref[s * w.q_per_seq:(s + 1) * w.q_per_seq] = o
+        ref_lse[s * w.q_per_seq:(s + 1) * w.q_per_seq] = l
+    check_out(out.float().cpu().numpy(), ref)
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() < 1e-3
 
 
 def test_prefill_bf16_cache_per_token_path():

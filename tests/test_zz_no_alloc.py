@@ -55,9 +55,12 @@ def _without_workspace(case):
 
 
 def test_noalloc_matches_decode_on_two_calls_in_a_row():
-    # two different problems back to back through the same scratch
+    # different problems back to back through the same scratch: one-token
+    # decode, speculative verify over NVFP4, and a small prefill chunk over FP8
+    # (the selection-list chain msa_decode runs for it)
     cases = [ms.make_case(ms.make_workload("fp8_decode", seq_lens=(9000, 3000, 700), seed=91), device="cuda"),
-             ms.make_case(ms.make_workload("nvfp4_verify", seq_lens=(4000, 2100), seed=92), device="cuda")]
+             ms.make_case(ms.make_workload("nvfp4_verify", seq_lens=(4000, 2100), seed=92), device="cuda"),
+             ms.make_case(ms.make_workload("fp8_prefill", seq_lens=(1300,), q_per_seq=24, seed=94), device="cuda")]
     for case in cases:
         t_ref, o_ref, l_ref = _with_workspace(case)
         t, o, l = _without_workspace(case)
@@ -68,8 +71,8 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
-    # 256 sequences with 8 new tokens each: one partial per (sequence, group) of
-    # 32 query x head columns is already 16 MiB, twice the scratch
+    # 256 sequences with 8 new tokens each: the workspace (pooled scores, the
+    # selection union, split partials) is larger than the scratch
     w = ms.make_workload("fp8_decode", seq_lens=(2048,) * 256, q_per_seq=8, seed=93)
     case = ms.make_case(w, device="cuda")
     cache, batch, iq, q = bind(case)
