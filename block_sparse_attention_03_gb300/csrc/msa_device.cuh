@@ -243,10 +243,12 @@ __device__ __forceinline__ int pow2_fit(float amax, float lim) {
   return e;
 }
 
-// Order-preserving map of a float to uint32 (NaN sorts as -inf - 1).
+// Order-preserving map of a float to uint32 (NaN sorts as -inf - 1; -0 and +0
+// map to one key, as they compare equal).
 __device__ __forceinline__ uint32_t float_order_key(float f) {
   if (f != f) return 0u;
   uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

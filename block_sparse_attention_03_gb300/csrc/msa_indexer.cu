@@ -22,9 +22,9 @@
 // column factor (query scale, power-of-two prescale, index scale, NVFP4
 // per-tensor scale: all positive) is applied after it.
 //
-// Work: unit = (sequence s, logical block b), b-major so that consecutive
-// units of a warp stay on one sequence when the warp count is a multiple of
-// the batch; units past a sequence's end write -inf.
+// Work: unit = (sequence s, logical block b) over the blocks that hold keys,
+// in sequence-major order, one contiguous run of units per warp; blocks past
+// a sequence's end get -inf in a separate spread pass.
 #include "msa_device.cuh"
 #include "msa_internal.h"
 #include "msa_qfrag.cuh"

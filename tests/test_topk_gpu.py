@@ -64,6 +64,11 @@ def _scores(rng, rows, max_blocks, kind):
         return rng.integers(0, 2, size=shape).astype(np.float32)
     if kind == "equal":
         return np.full(shape, 0.25, dtype=np.float32)
+    if kind == "signed_zero":  # +0 and -0 compare equal: ties between them keep the smaller id
+        x = rng.standard_normal(shape).astype(np.float32) * np.float32(0.1) - np.float32(1.0)
+        z = rng.random(shape) < 0.5
+        x[z] = np.where(rng.random(z.sum()) < 0.5, np.float32(0.0), np.float32(-0.0))
+        return x
     if kind == "neg_inf":  # masked scores mixed in
         x = rng.standard_normal(shape).astype(np.float32)
         x[rng.random(shape) < 0.7] = -np.inf
@@ -77,7 +82,7 @@ def _scores(rng, rows, max_blocks, kind):
     raise ValueError(kind)
 
 
-@pytest.mark.parametrize("kind", ["normal", "ties", "equal", "neg_inf", "near_ties"])
+@pytest.mark.parametrize("kind", ["normal", "ties", "equal", "neg_inf", "near_ties", "signed_zero"])
 def test_topk_short_rows(kind):
     rng = np.random.default_rng(100 + len(kind))
     seq_lens = [1, 128, 129, 700, 2049, 5000, 40000, 128 * 1000]
