@@ -324,3 +324,124 @@ def run_path(case: dict, topk=None, index_scale=None, sm_scale=None,
         o, l = attend_rows(case, s, sel, sm_scale)
         out[s * Q:(s + 1) * Q], lse[s * Q:(s + 1) * Q] = o, l
     return dict(pooled=pooled, topk=sel, out=out, lse=lse)
+
+
+# ----------------------------------------------------------------------------
+# cache insert (the step before the path): quantization of new tokens
+# ----------------------------------------------------------------------------
+#
+# vLLM Day-0 blog, section "QKV GEMM + norm + RoPE + KV 插入融合": the K, V and
+# index key of each new token are quantized and written straight into their
+# paged caches; "[M3] Enable FP8 sparse GQA" (items 1 and 4): the FP8 path
+# stores quantized values through the slot mapping.  Readings (the pages give
+# no formula): FP8 uses one fp32 scale per (token, head) row, amax / 448 (1 for
+# an all-zero row), and the codes round x / scale to nearest even, saturating at
+# +-448; NVFP4 uses the cache's fp32 per-tensor scale g (calibrated, given), an
+# e4m3 scale per 16 elements rounding amax16 / (6 g) to nearest even, and e2m1
+# codes rounding x / (scale * g) to nearest even, saturating at +-6, with a
+# value that rounds to zero stored as +0.  Every division and product is one
+# fp32 operation, as written.
+
+E4M3_MAX = 448.0
+E2M1_MAGS = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def e4m3_code(v) -> np.ndarray:
+    """OCP E4M3 code of fp32 values, round to nearest even, saturating at +-448.
+
+    The grid: 3 fraction bits; exponent floor(log2 |v|) for normals (>= 2^-6),
+    quantum 2^-9 below 2^-6 (subnormals).  The sign is kept (a negative value
+    that rounds to zero gives 0x80).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    quantum = np.exp2(e - 3.0)
+    q = a / quantum                      # exact (power-of-two quantum)
+    r = np.floor(q)
+    frac = q - r
+    r = np.where((frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1)), r + 1, r)
+    mag = np.minimum(r * quantum, E4M3_MAX)
+    # bits of the rounded magnitude
+    ee = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+    normal = mag >= 2.0 ** -6
+    exp_field = np.where(normal, ee + 7, 0).astype(np.int64)
+    man = np.where(normal, mag / np.exp2(ee) - 1.0, mag / 2.0 ** -9)
+    man_field = np.where(normal, np.round(man * 8), np.round(man)).astype(np.int64)
+    code = (exp_field << 3) | man_field
+    code = np.where(mag == 0, 0, code)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def e2m1_code(v) -> np.ndarray:
+    """FP4 E2M1 nibble of fp32 values: the nearest of 0, .5, 1, 1.5, 2, 3, 4, 6
+    (equal distance: the even code), saturating at 6; zero is stored as +0."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), 6.0)
+    mags = np.array(E2M1_MAGS)
+    d = np.abs(a[..., None] - mags)                     # distance to every magnitude
+    best = d.min(axis=-1, keepdims=True)
+    tie = d == best
+    # among the nearest codes take the even one (there are at most two)
+    even = tie & (np.arange(8) % 2 == 0)
+    code = np.where(even.any(axis=-1), even.argmax(axis=-1), tie.argmax(axis=-1))
+    return (code | np.where((v < 0) & (code > 0), 8, 0)).astype(np.uint8)
+
+
+def quantize_fp8_row(x):
+    """(codes uint8 [D], fp32 scale) of one bf16/fp32 row: scale = amax / 448."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.abs(x).max())
+    scale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    return e4m3_code((x / scale).astype(np.float32)), scale
+
+
+def quantize_nvfp4_row(x, gscale: float):
+    """(packed uint8 [D/2], e4m3 scale codes [D/16]) of one row with the given
+    fp32 per-tensor scale; element 2j in the low nibble of byte j."""
+    x = np.asarray(x, dtype=np.float32).reshape(-1, 16)
+    g = np.float32(gscale)
+    amax16 = np.abs(x).max(axis=1).astype(np.float32)
+    six_g = np.float32(np.float32(6.0) * g)
+    sf = e4m3_code((amax16 / six_g).astype(np.float32))
+    sfv = e4m3_value(sf).astype(np.float32)
+    denom = (sfv * g).astype(np.float32)
+    safe = np.where(denom > 0, denom, np.float32(1.0))
+    vals = np.where(denom[:, None] > 0, (x / safe[:, None]).astype(np.float32), np.float32(0.0))
+    nib = e2m1_code(vals).reshape(-1)
+    return (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), sf
+
+
+def insert_tokens(cache: dict, slots, k, v, index_k):
+    """Apply the insert of new tokens to a host copy of the caches (in place).
+
+    cache: dict with kv_dtype, index_dtype, and the arrays of the layout (k, v,
+    k_scale / k_sf, ..., idx, idx_scale / idx_sf) plus k_global, v_global,
+    idx_global.  slots[t] = physical block * 128 + offset (negative: skipped).
+    k, v: float32 [T][H][D] (bf16 values); index_k: float32 [T][Di] or None."""
+    for t, slot in enumerate(np.asarray(slots)):
+        if slot < 0:
+            continue
+        blk, off = divmod(int(slot), BLOCK)
+        for name, rows in (("k", k), ("v", v)):
+            dt = cache["kv_dtype"]
+            for h in range(rows.shape[1]):
+                _put_row(cache, name, dt, (blk, h, off), rows[t, h])
+        if index_k is not None:
+            _put_row(cache, "idx", cache["index_dtype"], (blk, off), index_k[t])
+
+
+def _put_row(cache, name, dt, where, row):
+    if dt == "bf16":
+        cache[name][where] = (np.asarray(row, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    elif dt == "fp8":
+        codes, scale = quantize_fp8_row(row)
+        cache[name][where] = codes
+        cache[name + "_scale"][where] = scale
+    elif dt == "nvfp4":
+        packed, sf = quantize_nvfp4_row(row, cache[name + "_global"])
+        cache[name][where] = packed
+        cache[name + "_sf"][where] = sf
+    else:
+        raise ValueError(dt)

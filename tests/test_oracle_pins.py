@@ -441,3 +441,109 @@ def test_full_topk_equals_dense_sdpa_with_fp8_queries_decoded_independently():
     ref = torch.nn.functional.scaled_dot_product_attention(
         qt, kt, vt, attn_mask=mask, scale=w.head_dim ** -0.5, enable_gqa=True)[0].permute(1, 0, 2).numpy()
     assert np.allclose(r["out"][:Q], ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- cache insert quantizers
+
+def test_e4m3_code_matches_torch_cast_in_range():
+    # round to nearest even on the OCP E4M3 grid, normals and subnormals, ties included
+    rng = np.random.default_rng(30)
+    v = (rng.standard_normal(100000) * np.exp2(rng.integers(-14, 9, 100000))).astype(np.float32)
+    mids = (O.e4m3_value(np.arange(0, 126, dtype=np.uint8)) + O.e4m3_value(np.arange(1, 127, dtype=np.uint8))) / 2
+    v = np.concatenate([v, mids.astype(np.float32), -mids.astype(np.float32), np.float32([0.0, -0.0])])
+    v = v[np.abs(v) <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_code(v), ref)
+
+
+def test_e4m3_code_saturates():
+    big = np.float32([448.0, 449.0, 464.0, 1e6, np.float32(3e38)])
+    assert np.all(O.e4m3_code(big) == 0x7E)
+    assert np.all(O.e4m3_code(-big) == 0xFE)
+
+
+def test_e2m1_code_is_the_nearest_magnitude_ties_to_even():
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    grid = np.arange(-7.0, 7.0, 1.0 / 64, dtype=np.float32)
+    got = O.e2m1_code(grid)
+    for x, c in zip(grid, got):
+        a = min(abs(float(x)), 6.0)
+        d = np.abs(a - mags)
+        near = np.flatnonzero(d == d.min())
+        want = near[0] if len(near) == 1 else [n for n in near if n % 2 == 0][0]
+        if x < 0 and want > 0:
+            want |= 8
+        assert c == want, (x, c, want)
+    # the tie points of the OCP FP4 grid by hand
+    ties = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for x, c in ties.items():
+        assert O.e2m1_code(np.float32(x)) == c and O.e2m1_code(np.float32(-x)) == (c | 8 if c else 0)
+
+
+def test_fp8_row_quantizer_scale_and_bound():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(128) * 0.3).astype(np.float32)
+    codes, scale = O.quantize_fp8_row(x)
+    amax = np.abs(x).max()
+    assert scale == np.float32(amax / np.float32(448.0))
+    back = O.e4m3_value(codes) * np.float64(scale)
+    assert np.all(np.abs(back - x) <= np.maximum(np.abs(x) * 2.0 ** -4, float(scale) * 2.0 ** -10) * (1 + 1e-6))
+    assert O.e4m3_value(codes[np.argmax(np.abs(x))]) in (448.0, -448.0)
+    codes0, scale0 = O.quantize_fp8_row(np.zeros(128, np.float32))
+    assert scale0 == 1.0 and np.all(codes0 == 0)
+
+
+def test_nvfp4_row_quantizer_recovers_representable_rows():
+    # x = e2m1 * e4m3 scale * g with a 6 in every group of 16: the quantizer must
+    # give back exactly these codes (nibble order: element 2j low)
+    rng = np.random.default_rng(32)
+    g = np.float32(0.0078125)
+    sf_codes = rng.integers(0x20, 0x60, size=8, dtype=np.uint8)
+    nib = rng.integers(0, 16, size=128, dtype=np.uint8)
+    nib[::16] = 7
+    nib[(nib & 7) == 0] = 0  # +0 only
+    x = (O.e2m1_value(nib) * np.repeat(O.e4m3_value(sf_codes), 16) * float(g)).astype(np.float32)
+    packed, sf = O.quantize_nvfp4_row(x, g)
+    assert np.array_equal(sf, sf_codes)
+    assert np.array_equal(packed & 0xF, nib[0::2]) and np.array_equal(packed >> 4, nib[1::2])
+
+
+def test_insert_writes_only_the_mapped_slots():
+    rng = np.random.default_rng(33)
+    H, D, nblk = 2, 128, 3
+    for kv in ("bf16", "fp8", "nvfp4"):
+        c = {"kv_dtype": kv, "index_dtype": kv, "k_global": 0.01, "v_global": 0.02, "idx_global": 0.005}
+        for name, shape in (("k", (nblk, H, 128)), ("v", (nblk, H, 128)), ("idx", (nblk, 128))):
+            if kv == "bf16":
+                c[name] = rng.integers(0, 1 << 16, size=shape + (D,), dtype=np.uint16)
+            elif kv == "fp8":
+                c[name] = rng.integers(0, 256, size=shape + (D,), dtype=np.uint8)
+                c[name + "_scale"] = rng.random(shape).astype(np.float32)
+            else:
+                c[name] = rng.integers(0, 256, size=shape + (D // 2,), dtype=np.uint8)
+                c[name + "_sf"] = rng.integers(0, 256, size=shape + (D // 16,), dtype=np.uint8)
+        before = {k2: v2.copy() for k2, v2 in c.items() if isinstance(v2, np.ndarray)}
+        slots = np.array([5, -1, 130, 383])
+        k = (rng.standard_normal((4, H, D)) * 0.1).astype(np.float32)
+        v = (rng.standard_normal((4, H, D)) * 0.1).astype(np.float32)
+        ik = (rng.standard_normal((4, D)) * 0.1).astype(np.float32)
+        k, v, ik = (torch.from_numpy(a).bfloat16().float().numpy() for a in (k, v, ik))
+        O.insert_tokens(c, slots, k, v, ik)
+        touched = {(0, 5), (1, 2), (2, 127)}
+        for name in ("k", "v", "idx"):
+            for blk in range(nblk):
+                for off in range(128):
+                    same = np.array_equal(c[name][blk, ..., off, :] if name == "idx" else c[name][blk, :, off],
+                                          before[name][blk, ..., off, :] if name == "idx" else before[name][blk, :, off])
+                    assert same == ((blk, off) not in touched), (kv, name, blk, off)
+        # the inserted values decode back within the format's bound
+        t, (blk, off) = 3, (2, 127)
+        for name, ref in (("k", k[t]), ("v", v[t])):
+            if kv == "bf16":
+                got = O.bf16_value(c[name][blk, :, off])
+            else:
+                got = O._dequant(kv, c[name][blk, :, off], scale=c.get(name + "_scale", np.ones((3, 2, 128)))[blk, :, off],
+                                 sf=c.get(name + "_sf", np.zeros((3, 2, 128, 8), np.uint8))[blk, :, off],
+                                 gscale=c[name + "_global"])
+            tol = 0 if kv == "bf16" else (0.07 if kv == "fp8" else 0.3)
+            assert np.abs(got - ref).max() <= tol * np.abs(ref).max() + 1e-12, (kv, name)
