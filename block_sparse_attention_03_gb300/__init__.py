@@ -27,7 +27,7 @@ DTYPES = {"bf16": 0, "fp8": 1, "nvfp4": 2}
 # every symbol include/msa.h declares
 EXPORTS = ("msa_workspace_size", "msa_workspace_init", "msa_indexer_score", "msa_topk_blocks",
            "msa_sparse_attend", "msa_decode", "msa_read_device_status", "msa_status_string",
-           "msa_dequant_debug", "msa_decode_noalloc")
+           "msa_dequant_debug", "msa_decode_noalloc", "msa_cache_insert")
 
 
 class MsaError(RuntimeError):
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         h.msa_status_string.argtypes = [ctypes.c_int]
         h.msa_dequant_debug.argtypes = [P, ctypes.c_int32, P, ctypes.c_int32, P, P]
         h.msa_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_int32, P, P, P, P, P]
+        h.msa_cache_insert.argtypes = [P, ctypes.c_int32, P, P, P, P, P, ctypes.c_size_t, P]
         for name in EXPORTS:
             if name != "msa_workspace_size" and name != "msa_status_string":
                 getattr(h, name).restype = ctypes.c_int
@@ -256,6 +257,15 @@ def msa_decode_noalloc(cache, batch, cfg, index_q: Query, q: Query, num_q_heads:
            "msa_decode_noalloc")
 
 
+def msa_cache_insert(cache, slot_mapping, k, v, index_k, workspace, stream=None) -> None:
+    """Quantize and write new tokens' K, V (bf16 [T][H][128]) and index keys (bf16
+    [T][128], or None) into the paged caches at slot_mapping (int32 [T])."""
+    c = cache.struct()
+    _check(lib().msa_cache_insert(_ref(c), int(slot_mapping.numel()), _ptr(slot_mapping), _ptr(k), _ptr(v),
+                                  _ptr(index_k), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "msa_cache_insert")
+
+
 def default_config(topk: int = 16, head_dim: int = 128, index_dim: int = 128) -> Config:
     """The model's settings: index and softmax scales head_dim ** -0.5."""
     return Config(topk=topk, index_scale=index_dim ** -0.5, sm_scale=head_dim ** -0.5)
@@ -264,4 +274,4 @@ def default_config(topk: int = 16, head_dim: int = 128, index_dim: int = 128) ->
 __all__ = ["PagedCache", "Batch", "Config", "Query", "MsaError", "lib", "EXPORTS", "default_config",
            "msa_workspace_size", "msa_workspace_init", "msa_indexer_score", "msa_topk_blocks",
            "msa_sparse_attend", "msa_decode", "msa_read_device_status", "msa_status_string",
-           "msa_dequant_debug", "msa_decode_noalloc", "roofline"]
+           "msa_dequant_debug", "msa_decode_noalloc", "msa_cache_insert", "roofline"]

@@ -581,6 +581,44 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, cons
   return run_attend(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st, true);
 }
 
+msa_status_t msa_cache_insert(const msa_cache_t* cache, int32_t num_tokens, const int32_t* slot_mapping,
+                              const void* k, const void* v, const void* index_k, void* workspace,
+                              size_t workspace_bytes, msa_stream_t stream) {
+  msa_status_t s;
+  if ((s = check_cache(cache, index_k != nullptr, true)) != MSA_OK) return s;
+  if (num_tokens < 0 || !workspace) return MSA_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < 256) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  if (num_tokens == 0) return MSA_OK;
+  if (!slot_mapping || !k || !v || !aligned16(k) || !aligned16(v) || (index_k && !aligned16(index_k)))
+    return MSA_ERR_INVALID_ARGUMENT;
+  InsertParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.num_tokens = num_tokens;
+  p.H = cache->num_kv_heads;
+  p.num_blocks = cache->num_blocks;
+  p.kv_fmt = fmt_of(cache->kv_dtype);
+  p.idx_fmt = index_k ? fmt_of(cache->index_dtype) : FMT_BF16;
+  p.slots = slot_mapping;
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.ik = static_cast<const __nv_bfloat16*>(index_k);
+  // the insert writes through the cache's pointers
+  p.kc = static_cast<uint8_t*>(const_cast<void*>(cache->k));
+  p.vc = static_cast<uint8_t*>(const_cast<void*>(cache->v));
+  p.ic = static_cast<uint8_t*>(const_cast<void*>(cache->idx));
+  p.ks = const_cast<float*>(cache->k_scale);
+  p.vs = const_cast<float*>(cache->v_scale);
+  p.is = const_cast<float*>(cache->idx_scale);
+  p.ksf = static_cast<uint8_t*>(const_cast<void*>(cache->k_sf));
+  p.vsf = static_cast<uint8_t*>(const_cast<void*>(cache->v_sf));
+  p.isf = static_cast<uint8_t*>(const_cast<void*>(cache->idx_sf));
+  p.kg = cache->k_global;
+  p.vg = cache->v_global;
+  p.ig = cache->idx_global;
+  p.status = static_cast<DeviceStatus*>(workspace);
+  return cuda_status(launch_insert(p, sm_count(), (cudaStream_t)stream));
+}
+
 msa_status_t msa_read_device_status(void* workspace, msa_stream_t stream, int32_t* detail) {
   if (!workspace) return MSA_ERR_INVALID_ARGUMENT;
   DeviceStatus h = {0, 0};

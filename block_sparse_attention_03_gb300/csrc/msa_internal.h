@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 #include "../../include/msa.h"
 
@@ -183,7 +184,23 @@ struct K2qParams {
   DeviceStatus* status;
 };
 
+// Cache insert of new tokens (bf16 rows in, the caches' formats out).
+struct InsertParams {
+  int32_t num_tokens, H, num_blocks;
+  int32_t kv_fmt, idx_fmt;
+  const int32_t* slots;       // [num_tokens] physical block * 128 + offset, < 0: skip
+  const __nv_bfloat16* k;     // [num_tokens][H][128]
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* ik;    // [num_tokens][128] or null
+  uint8_t *kc, *vc, *ic;      // cache data
+  float *ks, *vs, *is;        // FP8 per-token scales
+  uint8_t *ksf, *vsf, *isf;   // NVFP4 e4m3 scales
+  float kg, vg, ig;           // NVFP4 per-tensor scales
+  DeviceStatus* status;
+};
+
 // launchers (return cudaGetLastError())
+cudaError_t launch_insert(const InsertParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st);    // count, scan, fill
 cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms,
                               cudaStream_t st);

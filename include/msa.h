@@ -207,6 +207,38 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch,
                         void* out, float* lse, void* workspace, size_t workspace_bytes,
                         msa_stream_t stream);
 
+/* Cache insert: write the K, V and index key of num_tokens new tokens into
+ * the paged caches, quantized to the caches' formats -- the step just before
+ * the path (Day-0 blog, section "QKV GEMM + norm + RoPE + KV 插入融合": K, V and
+ * the index key are quantized and written straight into their caches; PR
+ * "[M3] Enable FP8 sparse GQA", items 1 and 4: FP8 values stored through the
+ * slot mapping).
+ * slot_mapping: device int32 [num_tokens]; token t goes to physical block
+ *   slot / 128, row slot % 128; negative entries are skipped (padding);
+ *   entries at or beyond num_blocks * 128 raise the device fault flag
+ *   (MSA_ERR_DEVICE_FAULT from msa_read_device_status) and are skipped.
+ * k, v: device bf16 [num_tokens][num_kv_heads][head_dim]; index_k: device bf16
+ *   [num_tokens][index_dim], or NULL to leave the index cache alone.  16-byte
+ *   aligned.
+ * Formats (per 128-element row, all arithmetic one fp32 operation each):
+ *   BF16   the bits are copied;
+ *   FP8    scale = amax / 448 (1 for an all-zero row) into k_scale / v_scale /
+ *          idx_scale, codes = E4M3(x / scale), round to nearest even,
+ *          saturating at +-448, the sign of a zero kept;
+ *   NVFP4  with the cache's per-tensor k_global / v_global / idx_global g
+ *          (the caller's calibrated scale), per 16 elements
+ *          sf = E4M3(amax16 / (6 g)) into k_sf / v_sf / idx_sf and codes =
+ *          E2M1(x / (sf * g)) (0 where sf * g = 0), round to nearest even,
+ *          saturating at +-6, a value that rounds to zero stored as +0;
+ *          element 2j in the low nibble of byte j.
+ * The call writes through the cache struct's data and scale pointers (they are
+ * declared const for the read-only entry points).  workspace: at least 256
+ * bytes; only its status word is used.  Rows of one token may be written in
+ * any order; two tokens mapped to one slot race. */
+msa_status_t msa_cache_insert(const msa_cache_t* cache, int32_t num_tokens, const int32_t* slot_mapping,
+                              const void* k, const void* v, const void* index_k, void* workspace,
+                              size_t workspace_bytes, msa_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's status word.
  * Returns MSA_OK, MSA_ERR_DEVICE_FAULT or MSA_ERR_TIMEOUT; *detail (optional,
  * host pointer) receives the raw flag bits. */

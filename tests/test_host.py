@@ -93,6 +93,11 @@ def test_bad_arguments_rejected_before_launch(lib):
     # a workspace that is too small
     assert lib.msa_decode(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), ctypes.byref(q), ctypes.byref(q), 16,
                           16, 16, None, ws, 300, None) == 3
+    # cache insert: null slot mapping, misaligned rows
+    assert lib.msa_cache_insert(ctypes.byref(c), 4, None, 16, 32, None, ws, 1 << 20, None) == 1
+    assert lib.msa_cache_insert(ctypes.byref(c), 4, 16, 17, 32, None, ws, 1 << 20, None) == 1
+    assert lib.msa_cache_insert(ctypes.byref(c), 4, 16, 16, 32, None, ws, 100, None) == 3
+    assert lib.msa_cache_insert(ctypes.byref(c), 0, None, None, None, None, ws, 1 << 20, None) == 0
     # e4m3 query without a scale
     qbad = msa.MsaQueryT(16, 1, 0.0)
     assert lib.msa_indexer_score(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), ctypes.byref(qbad), 16, ws,
