@@ -57,7 +57,10 @@ class MsaBatchT(ctypes.Structure):
 class MsaConfigT(ctypes.Structure):
     _fields_ = [("topk", ctypes.c_int32), ("init_blocks", ctypes.c_int32),
                 ("local_blocks", ctypes.c_int32), ("index_scale", ctypes.c_float),
-                ("sm_scale", ctypes.c_float)]
+                ("sm_scale", ctypes.c_float), ("score_type", ctypes.c_int32)]
+
+
+SCORE_TYPES = {"max": 0}  # msa_score_type_t: the block pooling of the index scores
 
 
 class MsaQueryT(ctypes.Structure):
@@ -162,9 +165,12 @@ class Config:
     local_blocks: int = 0
     index_scale: float = 128 ** -0.5
     sm_scale: float = 128 ** -0.5
+    score_type: str = "max"
 
     def struct(self) -> MsaConfigT:
-        return MsaConfigT(self.topk, self.init_blocks, self.local_blocks, self.index_scale, self.sm_scale)
+        # an unknown score type reaches the library as -1, which rejects it
+        return MsaConfigT(self.topk, self.init_blocks, self.local_blocks, self.index_scale, self.sm_scale,
+                          SCORE_TYPES.get(self.score_type, -1))
 
 
 @dataclasses.dataclass

@@ -93,6 +93,7 @@ msa_status_t check_cfg(const msa_config_t* c) {
     return MSA_ERR_INVALID_ARGUMENT;
   if (!(c->index_scale > 0.f) || !std::isfinite(c->index_scale)) return MSA_ERR_INVALID_ARGUMENT;
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale)) return MSA_ERR_INVALID_ARGUMENT;
+  if (c->score_type != MSA_SCORE_MAX) return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
 }
 

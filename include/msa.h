@@ -123,6 +123,15 @@ typedef struct {
   const int32_t* block_table;   /* device int32 [num_seqs][max_blocks_per_seq] */
 } msa_batch_t;
 
+/* How the per-key index scores of a block pool into the block's score: the
+ * indexer's score_type argument (API page "vllm.models.minimax_m3.nvidia.model",
+ * MiniMaxM3SparseAttention.__init__: score_type=sparse_cfg.get(
+ * "sparse_score_type", "max")).  The pages define only "max"; any other value
+ * returns MSA_ERR_UNSUPPORTED. */
+typedef enum {
+  MSA_SCORE_MAX = 0
+} msa_score_type_t;
+
 /* Method settings (the indexer's constructor arguments in the model). */
 typedef struct {
   int32_t topk;         /* blocks kept per (query, group): 4, 8, 16 or 32 */
@@ -130,6 +139,7 @@ typedef struct {
   int32_t local_blocks; /* blocks just before the query's own block always kept (default 0) */
   float index_scale;    /* multiplies the index scores; model: index_dim ** -0.5 */
   float sm_scale;       /* softmax scale; model: head_dim ** -0.5 */
+  int32_t score_type;   /* msa_score_type_t; 0 (max) in a zero-initialised struct */
 } msa_config_t;
 
 /* A query tensor: BF16, or FP8 E4M3 codes times one fp32 per-tensor scale. */

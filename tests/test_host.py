@@ -50,7 +50,7 @@ def _structs(**over):
     import block_sparse_attention_03_gb300 as msa
     c = msa.MsaCacheT(1, 1, 100, 128, 4, 128, 128, 16, 32, None, None, 48, 64, 80, None, 96, 0, 0, 0)
     b = msa.MsaBatchT(2, 1, 50, 16, 32)
-    f = msa.MsaConfigT(16, 0, 0, 128 ** -0.5, 128 ** -0.5)
+    f = msa.MsaConfigT(16, 0, 0, 128 ** -0.5, 128 ** -0.5, 0)
     for k, v in over.items():
         obj, field = k.split("__")
         setattr({"c": c, "b": b, "f": f}[obj], field, v)
@@ -62,7 +62,7 @@ def test_workspace_size_host_only(lib):
     n = lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 16)
     assert n > 0
     assert lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 15) == 0
-    for over in ({"f__topk": 12}, {"c__block_size": 64}, {"c__head_dim": 64}, {"b__num_seqs": 0},
+    for over in ({"f__topk": 12}, {"f__score_type": 1}, {"f__score_type": -1}, {"c__block_size": 64}, {"c__head_dim": 64}, {"b__num_seqs": 0},
                  {"f__init_blocks": 16}, {"b__q_per_seq": 50 * 128 + 1}, {"c__num_kv_heads": 9}):
         c2, b2, f2 = _structs(**over)
         assert lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) == 0, over
@@ -114,3 +114,18 @@ def test_prefill_workspace_holds_the_partials(lib):
     c2, b2, f2 = _structs(b__num_seqs=1, b__q_per_seq=8192, b__max_blocks_per_seq=576, c__num_blocks=600,
                           c__kv_dtype=2)
     assert 0 < lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) < n
+
+
+def test_score_type_other_than_max_is_unsupported(lib):
+    # the pages define only the "max" block pooling (the indexer's default
+    # score_type); any other value is refused before a launch
+    import block_sparse_attention_03_gb300 as msa
+    c, b, f = _structs(f__score_type=1)
+    q = msa.MsaQueryT(16, 0, 1.0)
+    ws = ctypes.c_void_p(4096)
+    assert lib.msa_indexer_score(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), ctypes.byref(q), 16, ws,
+                                 1 << 20, None) == 2
+    assert lib.msa_decode(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), ctypes.byref(q), ctypes.byref(q), 16,
+                          16, 16, None, ws, 1 << 20, None) == 2
+    assert msa.Config(score_type="mean").struct().score_type == -1
+    assert msa.Config().struct().score_type == 0
