@@ -224,7 +224,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
     pl.off_kent = o; o = align256(o + E * 4);
     pl.off_klist = o; o = align256(o + E * 4);
     pl.off_kpo = o; o = align256(o + P * 128 * 2);
-    pl.off_kpml = o; o = align256(o + P * 2 * 4);
+    pl.off_kpml = o; o = align256(o + P * 4 * 4);
   }
   pl.total = o;
   return MSA_OK;

@@ -1186,10 +1186,25 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
       for (int e = tid; e < -n * r; e += kK2qThreads) {
         const int ent = hdr[4 + e / r];
         const long part = ((long)(ent >> 5) * H + g * r + e % r) * K + (ent & 31);
-        p.part_ml[part * 2] = -INFINITY;
-        p.part_ml[part * 2 + 1] = 0.f;
+        p.part_ml[part * 4] = -INFINITY;
+        p.part_ml[part * 4 + 1] = 0.f;
+        p.part_ml[part * 4 + 2] = 1.f;
       }
     }
+    // o / l of a partial is bounded by the block's largest |v| <= 448 x its
+    // largest per-token V scale; a power of two 2^-ev brings that bound under
+    // 32768 so that the fp16 partials cannot overflow (ev = 0 for the usual
+    // scales), and 2^ev goes beside (m, l) for the combine
+    float vsm = 0.f;
+    if (n > 0) {
+      const float* vscl = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE + TR::KSC);
+      for (int k = lane; k < kBlock; k += 32) vsm = fmaxf(vsm, vscl[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) vsm = fmaxf(vsm, __shfl_xor_sync(0xffffffffu, vsm, o));
+    }
+    int ev = 0;
+    if (448.f * vsm > 32768.f) frexpf(448.f * vsm * (1.f / 32768.f), &ev);  // f * 2^ev, f in [0.5, 1)
+    const float vdown = ldexpf(1.f, -ev), vup = ldexpf(1.f, ev);
 #pragma unroll 1
     for (int ch = warp; ch * tpc < n; ch += 4) {
       const int ncol = min(tpc, n - ch * tpc) * r;  // real columns of this tile
@@ -1261,17 +1276,18 @@ __global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_co
         if (g8 == 0 && col < ncol) {
           const int ent = hdr[4 + ch * tpc + (col >> lr)];
           const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
-          p.part_ml[part * 2] = m_run[c];
-          p.part_ml[part * 2 + 1] = lsum;
+          p.part_ml[part * 4] = m_run[c];
+          p.part_ml[part * 4 + 1] = lsum;
+          p.part_ml[part * 4 + 2] = vup;
         }
       }
       __syncwarp();
       for (int col = 0; col < ncol; ++col) {
         const int ent = hdr[4 + ch * tpc + (col >> lr)];
         const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
-        // o / l in fp16 (|o / l| <= max |v|): half the bytes of the fp32 partial
+        // o / l x 2^-ev in fp16 (|o / l| <= max |v|): half the bytes of the fp32 partial
         const float lc = os[col * kMergeRow + 128];
-        const float inv = lc > 0.f ? __fdividef(1.f, lc) : 0.f;
+        const float inv = lc > 0.f ? __fdividef(1.f, lc) * vdown : 0.f;
         float v4[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {  // dim d = 4 lane + t from its accumulator row

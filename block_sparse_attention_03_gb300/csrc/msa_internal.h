@@ -177,8 +177,8 @@ struct K2qParams {
   const void* q;             // [S*Q][G*r][128]
   int32_t q_fp8;
   float q_scale, col_const;
-  uint16_t* part_o;          // [S*Q*G*r*topk][128] fp16 o / l of each (token, head, slot)
-  float* part_ml;            // [S*Q*G*r*topk][2]
+  uint16_t* part_o;          // [S*Q*G*r*topk][128] fp16 o / l x 2^-ev of each (token, head, slot)
+  float* part_ml;            // [S*Q*G*r*topk][4]: m, l, 2^ev, unused
   void* out;                 // bf16 [S*Q][G*r][128]
   float* lse;
   DeviceStatus* status;

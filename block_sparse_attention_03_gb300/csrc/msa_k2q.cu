@@ -8,7 +8,7 @@
 // and first attend item (kK2qTokens entries an item).  Fill: every entry
 // (token * 32 + slot) into its list, in arrival order (the per-entry results
 // do not depend on it).  The attend (msa_attend.cu) reads each item's K/V tile
-// once and writes one partial (o, m, l) per (token, head, slot); combine
+// once and writes one partial (o, m, l, 2^ev) per (token, head, slot); combine
 // merges a token's slots by log-sum-exp: the exact softmax over all of the
 // token's selected blocks (vLLM Day-0 blog, section "MSA 入门").
 #include "msa_device.cuh"
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
     // lane k < topk: slot k's (m, l); the row's max M and weights w_k = l_k 2^(m_k - M)
     // by warp reductions, then every slot's o / l loaded independently
-    float mk = -INFINITY, lk = 0.f;
+    float mk = -INFINITY, lk = 0.f, fk = 1.f;
     const int bl = lane < p.topk ? sel[lane] : -1;
     // a block an earlier slot already names has no list entry (k2q_list)
     const unsigned same = __match_any_sync(0xffffffffu, bl);
@@ -133,21 +133,24 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
       const int b = bl;
       if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
         const long part = row * p.topk + lane;
-        mk = __ldcg(p.part_ml + part * 2);
-        lk = __ldcg(p.part_ml + part * 2 + 1);
+        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + part);  // m, l, 2^ev
+        mk = ml.x;
+        lk = ml.y;
+        fk = ml.z;
       }
     }
     float M = mk;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float wk = (mk == -INFINITY) ? 0.f : k2q_ex2(mk - M) * lk;
+    const float wo = wk * fk;  // the weight of the stored o / l x 2^-ev
     float Lsum = wk;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
     for (int k = 0; k < p.topk; ++k) {
-      const float w = __shfl_sync(0xffffffffu, wk, k);
+      const float w = __shfl_sync(0xffffffffu, wo, k);
       if (w == 0.f) continue;  // warp-uniform
       const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + (row * p.topk + k) * 128) + lane);
       const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&pk.x));

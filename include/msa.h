@@ -152,9 +152,10 @@ typedef struct {
 /* Bytes of workspace msa_decode (and each of the other entry points) needs
  * for this problem.  Host-only; returns 0 for an invalid description.  A
  * prefill chunk (more than 8 new tokens a sequence) over an FP8 cache also
- * holds one partial per (token, q head, selected block) -- o / l in fp16, m and
- * l in fp32: 264 bytes x tokens x q heads x topk (554 MB for 8,192 tokens x 16
- * heads x 16). */
+ * holds one partial per (token, q head, selected block) -- o / l in fp16 (with
+ * a power-of-two scale that keeps it in range), m, l and that scale in fp32:
+ * 272 bytes x tokens x q heads x topk (571 MB for 8,192 tokens x 16 heads x
+ * 16). */
 size_t msa_workspace_size(const msa_cache_t* cache, const msa_batch_t* batch,
                           const msa_config_t* cfg, int32_t num_q_heads);
 

@@ -180,13 +180,23 @@ def test_full_size_sampled(name, seqs):
     w = ms.make_workload(name)
     c = ms.make_case(w, device="cuda")
     g = gpu_path(c)
+    # the pooled scores of the full-size launch too (the staged indexer entry point)
+    cache, batch, iq, _ = bind(c)
+    cfg = msa.default_config(w.topk)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    pooled_gpu = torch.empty((w.num_seqs * w.q_per_seq, w.num_kv_heads, w.max_blocks), dtype=torch.float32,
+                             device="cuda")
+    msa.msa_indexer_score(cache, batch, cfg, iq, pooled_gpu, ws)
+    assert msa.msa_read_device_status(ws)[0] == 0
+    pooled_gpu = pooled_gpu.cpu().numpy()
     h = ms.case_to_host(c)
-    del c
+    del c, ws
     torch.cuda.empty_cache()
     Q = w.q_per_seq
     for s in seqs:
         pooled = O.pooled_scores(h, s, w.index_dim ** -0.5)
         rows = list(range(s * Q, (s + 1) * Q))
+        check_pooled(pooled_gpu[rows], pooled)
         full = np.full((w.num_seqs * Q, w.num_kv_heads, w.max_blocks), -np.inf)
         full[rows] = pooled
         check_selection(g["topk"], full, w.seq_lens, Q, w.topk, rows=rows)
@@ -228,3 +238,41 @@ def test_full_size_prefill_sampled():
     check_selection(g["topk"], full, w.seq_lens, w.q_per_seq, w.topk, rows=rows)
     o, _ = O.attend_rows(h, 0, g["topk"], w.head_dim ** -0.5, rows=rows)
     check_out(g["out"][rows], o)
+
+
+def test_indexer_warps_with_more_than_32_blocks():
+    # 64 sequences of 128K tokens = 65,536 blocks over the persistent indexer's
+    # warps: each warp owns more than 32 blocks, so its window of 32 + 32 block
+    # facts slides during its run.  Only the index cache is built (1 GB of FP8
+    # keys); pooled scores of sampled sequences are checked against the oracle.
+    S, T = 64, 131072
+    nb = T // 128
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(61)
+    nblk = S * nb + 3
+    idx = torch.randint(0, 256, (nblk, 128, 128), dtype=torch.uint8, device="cuda", generator=gen)
+    idx[(idx & 0x7F) == 0x7F] = 0  # no NaN codes
+    idx_scale = torch.rand((nblk, 128), device="cuda", generator=gen) * 1e-3 + 1e-4
+    perm = torch.randperm(nblk, device="cuda", generator=gen)[: S * nb].int().reshape(S, nb)
+    lens = torch.full((S,), T, dtype=torch.int32, device="cuda")
+    lens[::3] -= 77  # ragged last blocks
+    iq = (torch.randn((S, 4, 128), device="cuda", generator=gen) / 11.3).bfloat16()
+    cache = msa.PagedCache(kv_dtype="fp8", index_dtype="fp8", num_blocks=nblk, num_kv_heads=4, k=idx, v=idx, idx=idx,
+                           idx_scale=idx_scale)
+    batch = msa.Batch(lens, perm, 1)
+    cfg = msa.default_config()
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    pooled = torch.empty((S, 4, nb), dtype=torch.float32, device="cuda")
+    msa.msa_indexer_score(cache, batch, cfg, msa.Query(iq), pooled, ws)
+    assert msa.msa_read_device_status(ws)[0] == 0
+    got = pooled.cpu().numpy()
+    w = ms.make_workload("fp8_long", seq_lens=tuple(int(x) for x in lens.cpu()), num_seqs=S)
+    rows = [0, 13, 31, 47, 63]
+    iq_host = iq.view(torch.int16).cpu().numpy().view(np.uint16)
+    for s in rows:
+        # the sequence's blocks gathered in logical order, under an identity table
+        h = {"workload": w, "seq_lens": lens.cpu().numpy(), "index_q": iq_host, "index_q_scale": 1.0,
+             "idx": idx[perm[s].long()].cpu().numpy(), "idx_scale": idx_scale[perm[s].long()].cpu().numpy(),
+             "block_table": np.arange(nb, dtype=np.int32)[None].repeat(S, axis=0)}
+        ref = O.pooled_scores(h, s, 128 ** -0.5)
+        check_pooled(got[[s]], ref)

@@ -248,3 +248,21 @@ def test_prefill_invisible_selection_flags_and_is_left_out():
     st, flags = msa.msa_read_device_status(ws)
     assert st != 0 and flags & 4
     assert torch.isfinite(out2.float()).all()
+
+
+def test_prefill_partials_with_large_v_scales():
+    # V per-token scales near 3e4 put |v| near 1e7, far above the fp16 range of
+    # the key-block-major partials (o / l <= max |v|): a power-of-two scale per
+    # partial must keep them finite.  Scaling every V scale by c scales the
+    # output by c, so the comparison is made on out / c.
+    from _helpers import check_out, gpu_path
+    w = ms.make_workload("fp8_prefill", seed=91, seq_lens=(1700,), q_per_seq=24)
+    c = ms.make_case(w, device="cuda")
+    mult = 1.0e7
+    c["v_scale"] *= mult
+    g = gpu_path(c)
+    assert np.isfinite(g["out"]).all()
+    h = ms.case_to_host(c)
+    o, lse = O.attend_rows(h, 0, g["topk"], w.head_dim ** -0.5)
+    check_out(g["out"] / mult, o / mult)
+    assert np.abs(g["lse"] - lse).max() < 1e-3
