@@ -193,18 +193,27 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
   for (int mt = 0; mt < MT; ++mt) {
     if constexpr (FMT == FMT_FP8 || FMT == FMT_BF16) {
       const int row = kw + 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+      // two accumulators per m tile (the query's hi and lo terms, or alternate
+      // k steps), summed at the end: MMA chains half as long
+      float sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < TR::QKS; ++ks) {
         uint32_t a[4];
         if constexpr (FMT == FMT_FP8) {
           ldmatrix_x4(a, swz(kt, row, 2 * ks + (lane >> 4)));
-#pragma unroll
-          for (int sp = 0; sp < SP; ++sp) mma_e4m3_k32(sacc[mt], a, QF(sp, ks, 0), QF(sp, ks, 1));
+          if constexpr (SP == 2) {
+            mma_e4m3_k32(sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
+            mma_e4m3_k32(sacc2, a, QF(1, ks, 0), QF(1, ks, 1));
+          } else {
+            mma_e4m3_k32((ks & 1) ? sacc2 : sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
+          }
         } else {
           ldmatrix_x4(a, swz(kt + (ks >> 2) * (128 * 128), row, 2 * (ks & 3) + (lane >> 4)));
-          mma_bf16_k16(sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
+          mma_bf16_k16((ks & 1) ? sacc2 : sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[mt][e] += sacc2[e];
     } else {
       const int r0 = kw + 16 * mt + g8, r1 = r0 + 8;
       const uint8_t* ksf = stg + TR::KTILE + TR::VTILE;
