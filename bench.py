@@ -423,6 +423,52 @@ def measure_workload(msa, B, st, steps, warmup, peak_gbs, peak_tf_e4m3):
     return res
 
 
+def measure_insert(msa, ms, B, peak_gbs, kv="fp8", tokens=65536):
+    """The cache insert of a prefill chunk's new tokens (bf16 K, V, index keys in;
+    the caches' formats out) timed alone: HBM-bound, algorithmic bytes = the bf16
+    rows read + the quantized rows and scales written."""
+    import torch
+    from block_sparse_attention_03_gb300 import roofline as R
+    H = 4
+    nblk = tokens // 128 + 8
+    w = ms.make_workload("tiny_bf16", seq_lens=(128,), kv_dtype=kv, index_dtype=kv, seed=5)
+    dev = B.dev
+    z8 = lambda *sh: torch.zeros(sh, dtype=torch.uint8, device=dev)
+    z32 = lambda *sh: torch.zeros(sh, dtype=torch.float32, device=dev)
+    if kv == "fp8":
+        cache = msa.PagedCache(kv_dtype=kv, index_dtype=kv, num_blocks=nblk, num_kv_heads=H, k=z8(nblk, H, 128, 128),
+                               v=z8(nblk, H, 128, 128), idx=z8(nblk, 128, 128), k_scale=z32(nblk, H, 128),
+                               v_scale=z32(nblk, H, 128), idx_scale=z32(nblk, 128))
+    else:
+        cache = msa.PagedCache(kv_dtype=kv, index_dtype=kv, num_blocks=nblk, num_kv_heads=H, k=z8(nblk, H, 128, 64),
+                               v=z8(nblk, H, 128, 64), idx=z8(nblk, 128, 64), k_sf=z8(nblk, H, 128, 8),
+                               v_sf=z8(nblk, H, 128, 8), idx_sf=z8(nblk, 128, 8), k_global=2.0 ** -10,
+                               v_global=2.0 ** -10, idx_global=2.0 ** -10)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6)
+    k = (torch.randn((tokens, H, 128), generator=gen, device=dev) * 0.1).bfloat16()
+    v = (torch.randn((tokens, H, 128), generator=gen, device=dev) * 0.1).bfloat16()
+    ik = (torch.randn((tokens, 128), generator=gen, device=dev) * 0.1).bfloat16()
+    # a prefill chunk's mapping: consecutive tokens fill consecutive rows of
+    # blocks taken from the pool in shuffled order
+    blocks = torch.randperm(nblk, generator=gen, device=dev)[:tokens // 128]
+    slots = (blocks[:, None] * 128 + torch.arange(128, device=dev)[None, :]).reshape(-1).int()
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    ms_ = B.time(lambda: msa.msa_cache_insert(cache, slots, k, v, ik, ws, B.stream), 20, warmup=3)
+    st, flags = msa.msa_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"insert: device status {flags}")
+    read = tokens * (2 * H * 128 * 2 + 128 * 2) + tokens * 4
+    written = tokens * (R.kv_bytes_per_token(kv, H) + R.index_bytes_per_token(kv))
+    written += tokens * (2 * H + 1) * 4 if kv == "fp8" else 0
+    gbs = (read + written) / (ms_ * 1e-3) / 1e9
+    del w
+    return {"kernel": "insert_kernel", "tokens": tokens, "cache": kv, "us": ms_ * 1e3,
+            "bytes": read + written, "achieved_gbs": gbs, "frac": gbs / peak_gbs,
+            "note": "bf16 rows read + quantized rows and their scales written; consecutive tokens to consecutive "
+                    "rows of shuffled blocks"}
+
+
 def dominant_roofline(res, peak_gbs, peak_tf, peak_kind):
     """The roofline of the stage that takes the most time alone (the top-k is
     bound by neither HBM nor the tensor pipe and never dominates)."""
@@ -579,6 +625,11 @@ def main():
             del sw
             torch.cuda.empty_cache()
 
+    insert = None
+    if rank == 0 and world == 1:
+        insert = {kv: measure_insert(msa, ms, B, peak, kv) for kv in ("fp8", "nvfp4")}
+        torch.cuda.empty_cache()
+
     cpu_base = None
     if pool is not None:
         plan, what = cpu_sample_plan(w)
@@ -609,6 +660,7 @@ def main():
             "gpu_launches": head["launches_per_step"] * args.steps,
             "clocks": clocks,
             "workloads": workloads,
+            "cache_insert": insert,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

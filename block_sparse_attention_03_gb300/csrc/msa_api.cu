@@ -588,6 +588,7 @@ msa_status_t msa_cache_insert(const msa_cache_t* cache, int32_t num_tokens, cons
   msa_status_t s;
   if ((s = check_cache(cache, index_k != nullptr, true)) != MSA_OK) return s;
   if (num_tokens < 0 || !workspace) return MSA_ERR_INVALID_ARGUMENT;
+  if (cache->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
   if (workspace_bytes < 256) return MSA_ERR_WORKSPACE_TOO_SMALL;
   if (num_tokens == 0) return MSA_OK;
   if (!slot_mapping || !k || !v || !aligned16(k) || !aligned16(v) || (index_k && !aligned16(index_k)))

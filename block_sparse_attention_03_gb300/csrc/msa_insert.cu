@@ -5,8 +5,9 @@
 // values stored through the slot mapping).  The projections, norms and RoPE
 // that precede it need weights and are not part of this library.
 //
-// One warp per row of 128 elements (a token's K head, V head or index key),
-// four elements a lane: an 8-byte load of the bf16 row piece, the row's or the
+// One warp per token, its rows of 128 elements (K heads, V heads, index key)
+// loaded together, four elements a lane: an 8-byte load of the bf16 row
+// piece, the row's or the
 // 16-group's absolute maximum by shuffles, one fp32 division per element, the
 // hardware's round-to-nearest-even conversions (cvt ... satfinite e4m3x2 /
 // e2m1x2), and coalesced stores of the codes.  The rules, fixed here because the
@@ -36,11 +37,10 @@ __device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
   return r;
 }
 
+// Quantize one row (raw: this lane's four bf16 elements) into the cache.
 template <int FMT>
-__device__ __forceinline__ void put_row(const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ data,
-                                        float* __restrict__ scale, uint8_t* __restrict__ sf, float g, long row,
-                                        int lane) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+__device__ __forceinline__ void put_row(const uint2 raw, uint8_t* __restrict__ data, float* __restrict__ scale,
+                                        uint8_t* __restrict__ sf, float g, long row, int lane) {
   if constexpr (FMT == FMT_BF16) {
     *reinterpret_cast<uint2*>(data + row * 256 + 8 * lane) = raw;
     return;
@@ -72,44 +72,64 @@ __device__ __forceinline__ void put_row(const __nv_bfloat16* __restrict__ src, u
   }
 }
 
-template <int KVF, int IF>
-__global__ void __launch_bounds__(32 * kInsertWarps) insert_kernel(const InsertParams p) {
+// One warp per token: the loads of all its rows (H K heads, H V heads, the
+// index key) are issued before any of them is quantized.  MAXH: the most
+// heads an instance handles (4: sixteen row registers, four CTAs an SM).
+template <int KVF, int IF, int MAXH>
+__global__ void __launch_bounds__(32 * kInsertWarps, MAXH == 4 ? 4 : 2) insert_kernel(const InsertParams p) {
+  constexpr int kMaxHeads = MAXH;
   const int lane = threadIdx.x & 31;
-  const int H = p.H, per_tok = 2 * H + (p.ik ? 1 : 0);
-  const long nrow = (long)p.num_tokens * per_tok;
-  for (long r = (long)blockIdx.x * kInsertWarps + (threadIdx.x >> 5); r < nrow;
-       r += (long)gridDim.x * kInsertWarps) {
-    const long t = r / per_tok;
-    const int j = (int)(r - t * per_tok);
+  const int H = p.H;
+  const long nw = (long)gridDim.x * kInsertWarps;
+  for (long t = (long)blockIdx.x * kInsertWarps + (threadIdx.x >> 5); t < p.num_tokens; t += nw) {
     const int slot = __ldg(p.slots + t);
-    if (slot < 0) continue;  // padding token
+    uint2 rk[kMaxHeads], rv[kMaxHeads], ri = make_uint2(0u, 0u);
+#pragma unroll
+    for (int h = 0; h < kMaxHeads; ++h) {
+      if (h < H) {
+        rk[h] = *reinterpret_cast<const uint2*>(p.k + (t * H + h) * kDim + 4 * lane);
+        rv[h] = *reinterpret_cast<const uint2*>(p.v + (t * H + h) * kDim + 4 * lane);
+      }
+    }
+    if (p.ik) ri = *reinterpret_cast<const uint2*>(p.ik + t * kDim + 4 * lane);
+    if (slot < 0) continue;  // a padding token
     const int blk = slot >> 7, off = slot & 127;
     if (blk >= p.num_blocks) {
-      if (lane == 0 && j == 0) raise_flag(p.status, FLAG_BAD_BLOCK, slot);
+      if (lane == 0) raise_flag(p.status, FLAG_BAD_BLOCK, slot);
       continue;
     }
-    if (j < H) {
-      put_row<KVF>(p.k + (t * H + j) * kDim, p.kc, p.ks, p.ksf, p.kg, ((long)blk * H + j) * kBlock + off, lane);
-    } else if (j < 2 * H) {
-      const int h = j - H;
-      put_row<KVF>(p.v + (t * H + h) * kDim, p.vc, p.vs, p.vsf, p.vg, ((long)blk * H + h) * kBlock + off, lane);
-    } else {
-      put_row<IF>(p.ik + t * kDim, p.ic, p.is, p.isf, p.ig, (long)blk * kBlock + off, lane);
+#pragma unroll
+    for (int h = 0; h < kMaxHeads; ++h) {
+      if (h < H) {
+        const long row = ((long)blk * H + h) * kBlock + off;
+        put_row<KVF>(rk[h], p.kc, p.ks, p.ksf, p.kg, row, lane);
+        put_row<KVF>(rv[h], p.vc, p.vs, p.vsf, p.vg, row, lane);
+      }
     }
+    if (p.ik) put_row<IF>(ri, p.ic, p.is, p.isf, p.ig, (long)blk * kBlock + off, lane);
   }
 }
 
 template <int KVF>
 cudaError_t launch_kv(const InsertParams& p, int num_sms, cudaStream_t st) {
-  const long rows = (long)p.num_tokens * (2 * p.H + (p.ik ? 1 : 0));
-  long grid = (rows + kInsertWarps - 1) / kInsertWarps;
-  const long cap = (long)(num_sms > 0 ? num_sms : 1) * 8;  // eight CTAs of 8 warps per SM walk the rest
+  long grid = ((long)p.num_tokens + kInsertWarps - 1) / kInsertWarps;
+  const long cap = (long)(num_sms > 0 ? num_sms : 1) * 16;  // the CTAs past those resident walk the rest
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
+  const bool h4 = p.H <= 4;
   switch (p.idx_fmt) {
-    case FMT_BF16: insert_kernel<KVF, FMT_BF16><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p); break;
-    case FMT_FP8: insert_kernel<KVF, FMT_FP8><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p); break;
-    case FMT_NVFP4: insert_kernel<KVF, FMT_NVFP4><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p); break;
+    case FMT_BF16:
+      if (h4) insert_kernel<KVF, FMT_BF16, 4><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      else insert_kernel<KVF, FMT_BF16, 8><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      break;
+    case FMT_FP8:
+      if (h4) insert_kernel<KVF, FMT_FP8, 4><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      else insert_kernel<KVF, FMT_FP8, 8><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      break;
+    case FMT_NVFP4:
+      if (h4) insert_kernel<KVF, FMT_NVFP4, 4><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      else insert_kernel<KVF, FMT_NVFP4, 8><<<(unsigned)grid, 32 * kInsertWarps, 0, st>>>(p);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
