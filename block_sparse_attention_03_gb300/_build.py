@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["msa_api.cu", "msa_indexer.cu", "msa_pindexer.cu", "msa_topk.cu", "msa_attend.cu", "msa_k2q.cu", "msa_dequant.cu",
+SOURCES = ["msa_api.cu", "msa_indexer.cu", "msa_pindexer.cu", "msa_topk.cu", "msa_attend.cu", "msa_k2q.cu", "msa_k2q_tc.cu", "msa_dequant.cu",
            "msa_insert.cu"]
 
 

@@ -153,7 +153,7 @@ struct Plan {
   // one partial per (token, head, slot), a combine pass)
   bool k2q = false;
   size_t off_kcnt = 0, off_koff = 0, off_kcur = 0, off_kitem = 0, off_kent = 0, off_klist = 0, off_kpo = 0,
-         off_kpml = 0;
+         off_kpml = 0, off_kq = 0, off_kqf = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -221,10 +221,13 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
     pl.off_koff = o; o = align256(o + L * 4);
     pl.off_kcur = o; o = align256(o + L * 4);
     pl.off_kitem = o; o = align256(o + (L + 1) * 4);
-    pl.off_kent = o; o = align256(o + E * 4);
+    pl.off_kent = o; o = align256(o + E * 4 + 16);  // the attend copies entries from 16-byte boundaries
     pl.off_klist = o; o = align256(o + E * 4);
     pl.off_kpo = o; o = align256(o + P * 128 * 2);
     pl.off_kpml = o; o = align256(o + P * 4 * 4);
+    const size_t R = (size_t)b->num_seqs * b->q_per_seq * hq;  // query rows (token, head)
+    pl.off_kq = o; o = align256(o + (q_fp8 ? 0 : R * 256));
+    pl.off_kqf = o; o = align256(o + (q_fp8 ? 0 : R * 4));
   }
   pl.total = o;
   return MSA_OK;
@@ -439,6 +442,7 @@ msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_confi
                      int hq, const int32_t* topk_idx, void* out, float* lse, const Plan& pl, void* ws,
                      cudaStream_t st) {
   const int G = c->num_kv_heads;
+  if (!aligned16(ws)) return MSA_ERR_INVALID_ARGUMENT;  // the attend's bulk copies read from it
   CUtensorMap tk, tv;
   const long rows = (long)c->num_blocks * G * kBlock;
   if (!encode_rows(&tk, c->k, rows, false) || !encode_rows(&tv, c->v, rows, false)) return MSA_ERR_CUDA;
@@ -459,12 +463,15 @@ msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_confi
   kp.item_off = at<int32_t>(ws, pl.off_kitem);
   kp.entries = at<int32_t>(ws, pl.off_kent);
   kp.item_list = at<int32_t>(ws, pl.off_klist);
+  kp.item_tokens = kBlock / kp.r;
   kp.k_scale = c->k_scale;
   kp.v_scale = c->v_scale;
   kp.q = q->data;
   kp.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
   kp.q_scale = kp.q_fp8 ? q->scale : 1.f;
   kp.col_const = cfg->sm_scale * 1.4426950408889634f;
+  kp.qsplit = at<uint8_t>(ws, pl.off_kq);
+  kp.qrowf = at<float>(ws, pl.off_kqf);
   kp.part_o = at<uint16_t>(ws, pl.off_kpo);
   kp.part_ml = at<float>(ws, pl.off_kpml);
   kp.out = out;

@@ -146,19 +146,6 @@ __device__ __forceinline__ int col_div(int col, int r) {
   return (int)(((float)col + 0.5f) * __frcp_rn((float)r));
 }
 
-// 2^e as a float for e in [-126, 127].
-__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
-
-// Largest e with v * 2^e <= 448 for a normal v > 0 (448 = 1.75 * 2^8), from
-// the exponent and mantissa fields; other v go the general way.
-__device__ __forceinline__ int fit448(float v) {
-  const uint32_t u = __float_as_uint(v);
-  const int be = (int)((u >> 23) & 0xffu);
-  if (!(v > 0.f) || be == 0 || be == 255) return pow2_fit(v, 448.f);
-  const int E = be - 127;
-  return ((u & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;
-}
-
 // Phases of attend_block: 1 logits, 2 softmax, 4 P tile, 8 O^T += V^T P.
 // A real block runs all of them; the dry run before the grid-dependency wait
 // gives each consumer warp one phase, so the four warps fetch the four parts
@@ -1085,260 +1072,6 @@ cudaError_t launch_att_fmt(const CUtensorMap* tk, const CUtensorMap* tv, const A
   }
 }
 
-// ---------------------------------------------------------------- key-block-major attend (prefill)
-//
-// Item = up to kK2qTokens entries (token, slot) of one list (sequence s, group
-// g, block b): the block's K/V tile is read once for all of them.  Four warps,
-// each owning one 8-column tile (8 / r tokens x r heads) of the item's
-// tokens at a time, run the one-block attend (attend_block, all 128 keys) and
-// write the unnormalised partial (o, m, l) of every (token, head) for that
-// slot; k2q_combine merges a token's slots.  Two stages: the next item's tile
-// is copied while this one is computed.
-constexpr int kK2qThreads = 128;
-
-template <int SP>
-struct K2qLayout {
-  using TR = AttTraits<FMT_FP8>;
-  static constexpr size_t TILES = (size_t)TR::KTILE + TR::VTILE + TR::KSC + TR::VSC;
-  static constexpr size_t STAGE = round_up(TILES, 1024);
-  static constexpr size_t FR = 2 * STAGE;                                   // query fragments, 4 tiles
-  static constexpr size_t FRW = (size_t)SP * 4 * TR::QKS * 64 * 4;
-  static constexpr size_t PSM = round_up(FR + FRW, 16);                     // per-warp P tiles
-  static constexpr size_t PSM_WARP = 64 * 32;
-  static constexpr size_t QO = PSM + 4 * PSM_WARP;                          // per-warp staging: q rows, then o
-  static constexpr size_t QO_WARP = 8 * kMergeRow * 4;  // 8 q rows (padded) or 8 o rows of kMergeRow
-  static constexpr size_t HDR = QO + 4 * QO_WARP;                           // [2] {n, s, g, b} + entries
-  static constexpr size_t HDR_STAGE = 16 + kK2qTokens * 4;
-  static constexpr size_t BARS = round_up(HDR + 2 * HDR_STAGE, 16);
-  static constexpr size_t TOTAL = BARS + 2 * 8;
-  static constexpr size_t SMEM = TOTAL + 1024;
-};
-
-template <int SP>
-__global__ void __launch_bounds__(kK2qThreads) k2q_attend_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                                 const __grid_constant__ CUtensorMap tmv,
-                                                                 const K2qParams p) {
-  using TR = AttTraits<FMT_FP8>;
-  using LY = K2qLayout<SP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + LY::BARS);
-  uint32_t* fr = reinterpret_cast<uint32_t*>(base + LY::FR);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = lane & 3, g8 = lane >> 2;
-  const BatchDev bt = p.batch;
-  const int G = p.G, r = p.r, H = G * r, Q = bt.Q, K = p.topk;
-  const int tpc = 8 / r;  // tokens per 8-column tile
-  const int lr = __ffs(r) - 1;  // r is 1, 2, 4 or 8: col / r = col >> lr
-  const long L = (long)bt.S * G * bt.max_nb;
-  const int items = p.item_off[L];
-
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-  }
-  __syncthreads();
-
-  // thread 0: item `it` into stage st (header, entries, K/V tile and scales)
-  auto issue = [&](int it, int st) {
-    const long list = p.item_list[it];
-    const int e0 = p.off[list] + (it - p.item_off[list]) * kK2qTokens;
-    const int n = min(kK2qTokens, p.off[list] + p.cnt[list] - e0);
-    const int s = (int)(list / ((long)G * bt.max_nb)), g = (int)((list / bt.max_nb) % G), b = (int)(list % bt.max_nb);
-    const int phys = bt.row(s)[b];
-    const bool ok = phys >= 0 && phys < p.num_blocks && n > 0;
-    int32_t* hdr = reinterpret_cast<int32_t*>(base + LY::HDR + (size_t)st * LY::HDR_STAGE);
-    hdr[0] = ok ? n : -n;  // negative: the block is rejected, its entries get empty partials
-    hdr[1] = s;
-    hdr[2] = g;
-    hdr[3] = b;
-    for (int e = 0; e < n; ++e) hdr[4 + e] = p.entries[e0 + e];
-    if (ok) {
-      uint8_t* stg = base + (size_t)st * LY::STAGE;
-      const size_t tile_id = (size_t)phys * G + g;
-      fence_proxy_async();
-      mbar_expect_tx(&bars[st], (uint32_t)LY::TILES);
-      tma_load_2d(stg, &tmk, 0, (int)(tile_id * kBlock), &bars[st]);
-      tma_load_2d(stg + TR::KTILE, &tmv, 0, (int)(tile_id * kBlock), &bars[st]);
-      bulk_g2s(stg + TR::KTILE + TR::VTILE, p.k_scale + tile_id * kBlock, TR::KSC, &bars[st]);
-      bulk_g2s(stg + TR::KTILE + TR::VTILE + TR::KSC, p.v_scale + tile_id * kBlock, TR::VSC, &bars[st]);
-    } else {
-      if (n > 0) raise_flag(p.status, FLAG_BAD_BLOCK, phys);
-      mbar_arrive(&bars[st]);  // an empty phase
-    }
-  };
-
-  int it = blockIdx.x;
-  if (tid == 0 && it < items) issue(it, 0);
-  int pending = it < items ? 1 : 0;  // thread 0: copies issued and not yet waited for
-#pragma unroll 1
-  for (int k = 0; it < items; ++k, it += gridDim.x) {
-    const int st = k & 1;
-    if (tid == 0 && it + (int)gridDim.x < items) {
-      issue(it + gridDim.x, st ^ 1);
-      ++pending;
-    }
-    const bool ok = mbar_wait(&bars[st], (uint32_t)((k >> 1) & 1));
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) raise_flag(p.status, FLAG_TIMEOUT, it);
-      break;
-    }
-    if (tid == 0) --pending;
-    const int32_t* hdr = reinterpret_cast<const int32_t*>(base + LY::HDR + (size_t)st * LY::HDR_STAGE);
-    const int n = hdr[0], s = hdr[1], g = hdr[2], b = hdr[3];
-    const int T = bt.seq_len(s);
-    const uint8_t* stg = base + (size_t)st * LY::STAGE;
-    if (n < 0) {  // rejected block: m = -inf, so that the combine leaves these slots out
-      for (int e = tid; e < -n * r; e += kK2qThreads) {
-        const int ent = hdr[4 + e / r];
-        const long part = ((long)(ent >> 5) * H + g * r + e % r) * K + (ent & 31);
-        p.part_ml[part * 4] = -INFINITY;
-        p.part_ml[part * 4 + 1] = 0.f;
-        p.part_ml[part * 4 + 2] = 1.f;
-      }
-    }
-    // o / l of a partial is bounded by the block's largest |v| <= 448 x its
-    // largest per-token V scale; a power of two 2^-ev brings that bound under
-    // 32768 so that the fp16 partials cannot overflow (ev = 0 for the usual
-    // scales), and 2^ev goes beside (m, l) for the combine
-    float vsm = 0.f;
-    if (n > 0) {
-      const float* vscl = reinterpret_cast<const float*>(stg + TR::KTILE + TR::VTILE + TR::KSC);
-      for (int k = lane; k < kBlock; k += 32) vsm = fmaxf(vsm, vscl[k]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) vsm = fmaxf(vsm, __shfl_xor_sync(0xffffffffu, vsm, o));
-    }
-    int ev = 0;
-    if (448.f * vsm > 32768.f) frexpf(448.f * vsm * (1.f / 32768.f), &ev);  // f * 2^ev, f in [0.5, 1)
-    const float vdown = ldexpf(1.f, -ev), vup = ldexpf(1.f, ev);
-#pragma unroll 1
-    for (int ch = warp; ch * tpc < n; ch += 4) {
-      const int ncol = min(tpc, n - ch * tpc) * r;  // real columns of this tile
-      // the tile's query rows into the warp's staging area with 16-byte loads
-      // (row col = 128 elements), then this warp's fragments (tile ct = warp)
-      // rows padded by 32 bytes: the 8 rows of a fragment load then start 8
-      // banks apart
-      uint8_t* qo = base + LY::QO + (size_t)warp * LY::QO_WARP;
-      const int esz = p.q_fp8 ? 1 : 2;
-      const int chunks = 128 * esz / 16;       // 16-byte pieces a row
-      const int qstride = 128 * esz + 32;      // bytes between staged rows
-      for (int e = lane; e < ncol * chunks; e += 32) {
-        const int col = e >> (p.q_fp8 ? 3 : 4), pc = e & (chunks - 1);  // chunks = 8 or 16
-        const long row = (long)(hdr[4 + ch * tpc + (col >> lr)] >> 5) * H + g * r + (col & (r - 1));
-        *reinterpret_cast<uint4*>(qo + (size_t)col * qstride + 16 * pc) =
-            *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + (size_t)row * 128 * esz + 16 * pc);
-      }
-      __syncwarp();
-      long rows[1];
-      rows[0] = g8 < ncol ? (long)g8 * (qstride / esz) : -1l;
-      uint32_t bq[SP][1][TR::QKS][2];
-      float cf[1][2];
-      build_qfrag<FMT_FP8, 1, SP, TR::QKS>(qo, p.q_fp8 != 0, rows, p.q_scale, p.col_const, bq, cf, lane);
-#pragma unroll
-      for (int sp = 0; sp < SP; ++sp)
-#pragma unroll
-        for (int ks = 0; ks < TR::QKS; ++ks)
-#pragma unroll
-          for (int rg = 0; rg < 2; ++rg) fr[(((sp * 4 + warp) * TR::QKS + ks) * 2 + rg) * 32 + lane] = bq[sp][0][ks][rg];
-      __syncwarp();
-      float colf[2], m_run[2], l_run[2], o[8][4];
-      int qlim[2], qbit[2] = {0, 0};
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col = 2 * j + c;
-        colf[c] = cf[0][c];
-        if (col < ncol) {
-          const int token = hdr[4 + ch * tpc + (col >> lr)] >> 5;
-          qlim[c] = T - Q + (token - s * Q);
-        } else {
-          qlim[c] = -1;
-        }
-        m_run[c] = -INFINITY;
-        l_run[c] = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) o[mm][c] = o[mm][c + 2] = 0.f;
-      }
-      int e_prev = 0;
-      attend_block<FMT_FP8, 4, SP>(stg, base + LY::PSM + (size_t)warp * LY::PSM_WARP, nullptr, fr, warp, colf, qlim,
-                                   qbit, 1u, b * kBlock, 0, warp, lane, m_run, l_run, o, e_prev, kAllPhases);
-      // the partial of every (token, head) column for this slot: o through the
-      // staging area (the query rows are no longer needed) in accumulator-row
-      // order with padded rows (conflict-free stores), then one 512-byte row a
-      // column
-      const float oscale = (e_prev >= -126 && e_prev <= 126) ? pow2i(-e_prev) : ldexpf(1.f, -e_prev);
-      float* os = reinterpret_cast<float*>(qo);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float lsum = l_run[c];
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-        const int col = 2 * j + c;
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm)
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) os[col * kMergeRow + 16 * mm + 8 * h2 + g8] = o[mm][c + 2 * h2] * oscale;
-        if (g8 == 0) os[col * kMergeRow + 128] = lsum;  // the row's padding holds its l
-        if (g8 == 0 && col < ncol) {
-          const int ent = hdr[4 + ch * tpc + (col >> lr)];
-          const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
-          p.part_ml[part * 4] = m_run[c];
-          p.part_ml[part * 4 + 1] = lsum;
-          p.part_ml[part * 4 + 2] = vup;
-        }
-      }
-      __syncwarp();
-      for (int col = 0; col < ncol; ++col) {
-        const int ent = hdr[4 + ch * tpc + (col >> lr)];
-        const long part = ((long)(ent >> 5) * H + g * r + (col & (r - 1))) * K + (ent & 31);
-        // o / l x 2^-ev in fp16 (|o / l| <= max |v|): half the bytes of the fp32 partial
-        const float lc = os[col * kMergeRow + 128];
-        const float inv = lc > 0.f ? __fdividef(1.f, lc) * vdown : 0.f;
-        float v4[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {  // dim d = 4 lane + t from its accumulator row
-          const int d = 4 * lane + t, q = d >> 4, rem = d & 15;
-          const int gg = ((q & 3) << 1) | (q >> 2);
-          v4[t] = os[col * kMergeRow + 16 * (rem >> 1) + 8 * (rem & 1) + gg] * inv;
-        }
-        uint2 pk;
-        pk.x = pack_f16x2(v4[0], v4[1]);
-        pk.y = pack_f16x2(v4[2], v4[3]);
-        reinterpret_cast<uint2*>(p.part_o + part * 128)[lane] = pk;
-      }
-      __syncwarp();
-    }
-    __syncthreads();  // the stage and the fragments are free again
-  }
-  // a CTA that gave up waits (bounded) for the copies it issued
-  if (tid == 0) {
-    for (int q2 = 0; q2 < pending && q2 < 2; ++q2) mbar_wait(&bars[q2], 0, 2000);
-  }
-}
-
-template <int SP>
-cudaError_t launch_k2q(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms, cudaStream_t st) {
-  const size_t smem = K2qLayout<SP>::SMEM;
-  auto kern = k2q_attend_kernel<SP>;
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kK2qThreads, smem);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
-  const int grid = per_sm * (num_sms > 0 ? num_sms : 1);
-  kern<<<grid, kK2qThreads, smem, st>>>(*tk, *tv, p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_attend(int fmt, const CUtensorMap* tk, const CUtensorMap* tv, const AttendParams& p, int num_sms,
@@ -1349,11 +1082,6 @@ cudaError_t launch_attend(int fmt, const CUtensorMap* tk, const CUtensorMap* tv,
     case FMT_NVFP4: return launch_att_fmt<FMT_NVFP4>(tk, tv, p, num_sms, st, pdl);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms,
-                              cudaStream_t st) {
-  return p.q_fp8 ? launch_k2q<1>(tk, tv, p, num_sms, st) : launch_k2q<2>(tk, tv, p, num_sms, st);
 }
 
 }  // namespace msa

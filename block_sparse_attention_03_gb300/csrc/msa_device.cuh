@@ -243,6 +243,19 @@ __device__ __forceinline__ int pow2_fit(float amax, float lim) {
   return e;
 }
 
+// 2^e as a float for e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Largest e with v * 2^e <= 448 for a normal v > 0 (448 = 1.75 * 2^8), from
+// the exponent and mantissa fields; other v go the general way.
+__device__ __forceinline__ int fit448(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const int be = (int)((u >> 23) & 0xffu);
+  if (!(v > 0.f) || be == 0 || be == 255) return pow2_fit(v, 448.f);
+  const int E = be - 127;
+  return ((u & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;
+}
+
 // Order-preserving map of a float to uint32 (NaN sorts as -inf - 1; -0 and +0
 // map to one key, as they compare equal).
 __device__ __forceinline__ uint32_t float_order_key(float f) {

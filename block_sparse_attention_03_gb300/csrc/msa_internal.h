@@ -160,7 +160,6 @@ struct PrefillIndexerParams {
 
 // Key-block-major attend of prefill chunks (the selections inverted into one
 // list per (sequence, group, block) of the (token, slot) pairs that chose it).
-constexpr int kK2qTokens = 16;  // tokens per attend item (one K/V tile read for all of them)
 struct K2qParams {
   BatchDev batch;            // the real batch: S sequences, Q new tokens each
   int32_t G, r, topk;
@@ -172,11 +171,14 @@ struct K2qParams {
   int32_t* item_off;         // [L + 1] first attend item of each list; [L] = items in all
   int32_t* entries;          // [S*Q*G*topk] token * 32 + slot, list by list
   int32_t* item_list;        // [S*Q*G*topk] (at most one item per entry) the list of each attend item
+  int32_t item_tokens;       // entries (tokens) per attend item: 128 / r, one MMA row per (token, head)
   const float* k_scale;      // FP8 per-token scales
   const float* v_scale;
   const void* q;             // [S*Q][G*r][128]
   int32_t q_fp8;
   float q_scale, col_const;
+  uint8_t* qsplit;           // bf16 query: [S*Q*G*r][2][128] e4m3 hi, lo terms of q x 2^e (per row)
+  float* qrowf;              // [S*Q*G*r] 2^-e x col_const
   uint16_t* part_o;          // [S*Q*G*r*topk][128] fp16 o / l x 2^-ev of each (token, head, slot)
   float* part_ml;            // [S*Q*G*r*topk][4]: m, l, 2^ev, unused
   void* out;                 // bf16 [S*Q][G*r][128]

@@ -4,13 +4,15 @@
 // per-block partials.
 //
 // Count: for every (token, group, slot) whose selected block is b, one more
-// entry in list (sequence, group, b).  Scan (one CTA): each list's first entry
-// and first attend item (kK2qTokens entries an item).  Fill: every entry
-// (token * 32 + slot) into its list, in arrival order (the per-entry results
-// do not depend on it).  The attend (msa_attend.cu) reads each item's K/V tile
-// once and writes one partial (o, m, l, 2^ev) per (token, head, slot); combine
-// merges a token's slots by log-sum-exp: the exact softmax over all of the
-// token's selected blocks (vLLM Day-0 blog, section "MSA 入门").
+// entry in list (sequence, group, b); the same pass splits each bf16 query row
+// into the e4m3 hi + lo terms the attend's MMA reads.  Scan (one CTA): each
+// list's first entry and first attend item (item_tokens = 128 / r entries an
+// item: one MMA row per (token, head)).  Fill: every entry (token * 32 + slot)
+// into its list, in arrival order (the per-entry results do not depend on
+// it).  The attend (msa_k2q_tc.cu) reads each item's K/V tile once and writes
+// one partial (o, m, l, 2^ev) per (token, head, slot); combine merges a
+// token's slots by log-sum-exp: the exact softmax over all of the token's
+// selected blocks (vLLM Day-0 blog, section "MSA 入门").
 #include "msa_device.cuh"
 #include "msa_internal.h"
 
@@ -48,6 +50,33 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
     const long key = k2q_list(p, e, true);
     if (key >= 0) atomicAdd(&p.cnt[key], 1);
   }
+  if (p.q_fp8) return;
+  // bf16 query rows (token, head), a warp each, lane l holding dims 4l .. 4l+3:
+  // q x 2^e with the largest e that keeps the row's amax at most 448 (exact),
+  // split into e4m3 hi + lo (together all 8 significant bits of bf16), and
+  // the row factor 2^-e x col_const
+  const long rows = (long)bt.S * bt.Q * p.G * p.r;
+  const int lane = threadIdx.x & 31;
+  const long nw = (long)gridDim.x * (blockDim.x >> 5);
+  for (long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q) + row * 128) + lane);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int ex = pow2_fit(amax, 448.f);
+    const float ps = ldexpf(1.f, ex);
+    float h[4], l[4];
+    split_e4m3(a.x * ps, h[0], l[0]);
+    split_e4m3(a.y * ps, h[1], l[1]);
+    split_e4m3(b.x * ps, h[2], l[2]);
+    split_e4m3(b.y * ps, h[3], l[3]);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.qsplit + row * 256);
+    dst[lane] = (uint32_t)pack_e4m3x2(h[0], h[1]) | ((uint32_t)pack_e4m3x2(h[2], h[3]) << 16);
+    dst[32 + lane] = (uint32_t)pack_e4m3x2(l[0], l[1]) | ((uint32_t)pack_e4m3x2(l[2], l[3]) << 16);
+    if (lane == 0) p.qrowf[row] = ldexpf(1.f, -ex) * p.col_const;
+  }
 }
 
 // One CTA of 1024 threads: thread t owns the contiguous lists [t*L/1024, (t+1)*L/1024).
@@ -61,7 +90,7 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
   for (long i = l0; i < l1; ++i) {
     const int c = p.cnt[i];
     ne += c;
-    ni += (c + kK2qTokens - 1) / kK2qTokens;
+    ni += (c + p.item_tokens - 1) / p.item_tokens;
   }
   se[t] = ne;
   si[t] = ni;
@@ -76,7 +105,7 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
   int e0 = se[t] - ne, i0 = si[t] - ni;
   for (long i = l0; i < l1; ++i) {
     const int c = p.cnt[i];
-    const int items = (c + kK2qTokens - 1) / kK2qTokens;
+    const int items = (c + p.item_tokens - 1) / p.item_tokens;
     p.off[i] = e0;
     p.cur[i] = e0;
     p.item_off[i] = i0;

@@ -154,8 +154,9 @@ typedef struct {
  * prefill chunk (more than 8 new tokens a sequence) over an FP8 cache also
  * holds one partial per (token, q head, selected block) -- o / l in fp16 (with
  * a power-of-two scale that keeps it in range), m, l and that scale in fp32:
- * 272 bytes x tokens x q heads x topk (571 MB for 8,192 tokens x 16 heads x
- * 16). */
+ * 272 bytes x tokens x q heads x topk, and with a bf16 query its rows as two
+ * e4m3 terms and a factor: 260 bytes x tokens x q heads (605 MB in all for
+ * 8,192 tokens x 16 heads x 16). */
 size_t msa_workspace_size(const msa_cache_t* cache, const msa_batch_t* batch,
                           const msa_config_t* cfg, int32_t num_q_heads);
 
