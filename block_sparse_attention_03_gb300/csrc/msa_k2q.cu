@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     if (lane < p.topk) {
       const int b = bl;
       if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
-        const long part = row * p.topk + lane;
+        const long part = (token * p.topk + lane) * H + h;
         const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + part);  // m, l, 2^ev
         mk = ml.x;
         lk = ml.y;
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     for (int k = 0; k < p.topk; ++k) {
       const float w = __shfl_sync(0xffffffffu, wo, k);
       if (w == 0.f) continue;  // warp-uniform
-      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + (row * p.topk + k) * 128) + lane);
+      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + ((token * p.topk + k) * H + h) * 128) + lane);
       const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&pk.x));
       const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&pk.y));
       acc.x += w * o01.x;

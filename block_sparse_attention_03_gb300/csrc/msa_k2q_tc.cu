@@ -15,26 +15,35 @@
 // 128 / r tokens.
 //
 // Item = up to 128 / r entries of one list, as 128 MMA rows (entry, head):
-//   S[128 x 128 keys] = Qop[128 x 128 dims] . K^T       (MMA 1, K-major both)
-//   O[128 x 128 dims] = P[128 x 128 keys] . V           (MMA 2, V MN-major)
+//   S[128 x 128 keys] = Qop[128 x 128 dims] . K^T    (MMA 1: A, B in shared memory, K-major)
+//   O[128 x 128 dims] = P[128 x 128 keys] . V        (MMA 2: A = P in TMEM, B = V MN-major)
 // kind::f8f6f4, e4m3 x e4m3, fp32 accumulators in TMEM.  A bf16 query enters
 // as two e4m3 terms (hi + lo, after a power-of-two scale per row, prepared
 // once per (token, head) by the count pass); an e4m3 query as one.  P enters as
-// hi + lo e4m3 terms of p * vscale_t * 2^e (2^e puts the block's largest V
-// scale at most at 448), so that V's per-token scales fold into P.
+// hi + lo e4m3 terms of p * 2^e * vscale_t (2^e puts the block's largest V
+// scale at most at 448), so that V's per-token scales fold into P; 2^e rides
+// in the exponent of p, and l is summed at the same scale, so that o / l needs
+// no further factor.  P is written into the S columns already read (hi and lo
+// of each 32-key chunk side by side), where MMA 2 takes its A operand.
 //
 // One CTA per SM (all 512 TMEM columns), 9 warps:
-//   warp 0     copies items (header, entries, K / V tiles with the 128-byte
-//              swizzle, per-token scales) into a 4-stage ring, the facts of 32
-//              items at a time read by its 32 lanes together; owns TMEM;
+//   warp 0     writes item headers (list facts, the entries by bulk copy) into
+//              an 8-slot ring two items ahead of the K / V tiles, which it
+//              copies (TMA, 128-byte swizzle, with the per-token scales) into a
+//              4-stage ring; the facts of 32 items at a time are read by its 32
+//              lanes together; it owns TMEM;
 //   warps 1-4  group 0 and warps 5-8 group 1 take alternate items; each
-//              thread owns one MMA row (TMEM lane).  A group builds its
-//              item's query operand, its leader thread issues MMA 1, the
-//              threads turn S into P in the same shared buffer (max, exp2,
-//              sum, V scales, hi / lo split), the leader issues MMA 2, and
-//              while it runs the group loads its next item's query rows; the
-//              next item's MMA 1 is issued before this item's output is
-//              written.  S (128 columns) and O (128 columns) per group.
+//              thread owns one MMA row (TMEM lane).  Once its item's logits are
+//              in TMEM a group starts the copies of its next item's query rows
+//              (cp.async, a warp's 32 rows together, whole rows per
+//              instruction) into the operand buffer MMA 1 has finished with,
+//              turns S into P (max, exp2, sum, V scales, hi / lo split), and
+//              its leader thread issues MMA 2; when O is ready the leader
+//              issues the next item's MMA 1, and the group writes this item's
+//              output: fp16 rows staged in the item's (now free) stage, one
+//              bulk copy per entry (its r heads are adjacent in the partials),
+//              after which the group's threads release the stage.  S (then P)
+//              and O take 128 columns each per group.
 // Every wait is bounded; a wait that gives up sets the timeout flag and the
 // CTA stops issuing, drains what it issued and frees its TMEM.
 #include "msa_device.cuh"
@@ -45,31 +54,37 @@ namespace msa {
 
 namespace {
 
-constexpr int kTqStages = 4;
+constexpr int kTqStages = 4;               // K / V stages (two per group)
+constexpr int kTqHdrs = 8;                 // header slots
+constexpr int kTqAhead = 2;                // headers written this many items before their tiles
 constexpr int kTqThreads = 288;
-constexpr uint32_t kTqTile = 128 * 128;   // one e4m3 128 x 128 operand
+constexpr uint32_t kTqTile = 128 * 128;    // one e4m3 128 x 128 operand
 constexpr uint32_t kTqScales = 128 * 4;
-constexpr uint32_t kTqEnt = 136 * 4;      // an item's entries, copied from a 16-byte boundary
-constexpr uint32_t kTqHdr = 8 * 4;
+constexpr uint32_t kTqEnt = 136 * 4;       // an item's entries, copied from a 16-byte boundary
+constexpr uint32_t kTqHdrW = 8;            // header words
 
 constexpr uint32_t tq_round(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 struct TqLayout {
-  static constexpr uint32_t OP = 0;                         // [group][hi, lo][16 KB]: query operand, then P
-  static constexpr uint32_t ST = OP + 4 * kTqTile;          // the ring of stages
+  static constexpr uint32_t OP = 0;                          // [group][hi, lo][16 KB] query operand
+  static constexpr uint32_t ST = OP + 4 * kTqTile;           // the ring of stages
   static constexpr uint32_t S_K = 0, S_V = kTqTile, S_KS = 2 * kTqTile, S_VS = S_KS + kTqScales;
-  static constexpr uint32_t S_ENT = S_VS + kTqScales, S_HDR = S_ENT + kTqEnt;
-  static constexpr uint32_t STAGE = tq_round(S_HDR + kTqHdr, 1024);
-  static constexpr uint32_t BARS = ST + kTqStages * STAGE;
-  // kvfull[stages], kvempty[stages], sbar[2], obar[2], done[2]
-  static constexpr uint32_t NBARS = 2 * kTqStages + 6;
+  // the output rows of an item, staged after MMA 2: 128 / r entries of r rows
+  // of 256 bytes, 16 bytes apart (conflict-free stores)
+  static constexpr uint32_t STAGE = tq_round(S_VS + kTqScales + 2048, 1024);
+  static constexpr uint32_t HD = ST + kTqStages * STAGE;     // header slots: entries, then words
+  static constexpr uint32_t HSLOT = kTqEnt + kTqHdrW * 4;
+  static constexpr uint32_t BARS = tq_round(HD + kTqHdrs * HSLOT, 16);
+  // kvfull[stages], kvempty[stages], hfull[slots], hempty[slots], sbar[2], obar[2], done[2]
+  static constexpr uint32_t NBARS = 2 * kTqStages + 2 * kTqHdrs + 6;
   static constexpr uint32_t TSLOT = BARS + NBARS * 8;
   static constexpr uint32_t DEAD = TSLOT + 4;
   static constexpr uint32_t TOTAL = DEAD + 12;
-  static constexpr uint32_t SMEM = TOTAL + 1024;            // 1024-byte alignment slack
+  static constexpr uint32_t SMEM = TOTAL + 1024;             // 1024-byte alignment slack
 };
+static_assert(TqLayout::STAGE >= 32768 + 128 * 16, "an item's output rows fit its stage");
 
-// Instruction descriptors: D fp32, A and B e4m3, M = N = 128; A K-major; B
+// Instruction descriptors: D fp32, A and B e4m3, M = N = 128, A K-major; B
 // K-major (keys, MMA 1) or MN-major (V with the head dims contiguous, MMA 2).
 constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
@@ -83,20 +98,61 @@ __device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// D (TMEM) = / += A (TMEM, K-major rows = lanes) x B (smem)^T, e4m3, fp32 accumulate.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16-byte global -> shared copy (zero fill when !ok), completed by cp_async_wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float tq_ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
+// (a, b) as two e4m3 terms, hi + lo, through f16 (a in the low byte of each):
+// hi = e4m3(f16(x)), lo = e4m3(f16(x) - hi), the difference exact in f16.
+__device__ __forceinline__ void split2_e4m3(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint32_t h2 = pack_f16x2(a, b);
+  uint16_t h8, l8;
+  uint32_t back;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(h2));
+  asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(back) : "h"(h8));
+  const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(*reinterpret_cast<const uint32_t*>(&d)));
+  hi = h8;
+  lo = l8;
+}
+
 // This thread's row of an item.
 struct TqRow {
-  int st;       // ring stage
+  int hs;       // header slot
+  int st;       // K / V stage
   int valid;    // the row holds a real (entry, head)
   int pos;      // last key the row's token may see (-1: none)
   int key0;     // the block's first key
-  long part;    // (token, head, slot) partial
-  long qrow;    // (token, head) query row
+  int qrow;     // (token, head) query row
+  long part;    // (token, slot, head) partial
 };
 
 __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -107,7 +163,9 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
   using LY = TqLayout;
   uint64_t* kvfull = reinterpret_cast<uint64_t*>(base + LY::BARS);
   uint64_t* kvempty = kvfull + kTqStages;
-  uint64_t* sbar = kvempty + kTqStages;
+  uint64_t* hfull = kvempty + kTqStages;
+  uint64_t* hempty = hfull + kTqHdrs;
+  uint64_t* sbar = hempty + kTqHdrs;
   uint64_t* obar = sbar + 2;
   uint64_t* done = obar + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + LY::TSLOT);
@@ -126,7 +184,11 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTqStages; ++i) {
       mbar_init(&kvfull[i], 1);
-      mbar_init(&kvempty[i], 1);
+      mbar_init(&kvempty[i], 128);  // the item's group, thread by thread
+    }
+    for (int i = 0; i < kTqHdrs; ++i) {
+      mbar_init(&hfull[i], 1);
+      mbar_init(&hempty[i], 128);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sbar[i], 1);
@@ -145,13 +207,21 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
   const uint32_t tmem = *tslot;
 
   if (warp == 0) {
-    // ---------------- items into the ring
-    int issued = 0;
+    // ---------------- headers, then (kTqAhead items later) tiles.  Step t
+    // writes header t and copies the tiles of item t - kTqAhead; the tile
+    // step reads the item's block from its header slot, which the producer
+    // alone writes and does not reuse before header t - kTqAhead + kTqHdrs.
+    int issued_h = 0, issued_k = 0;
     bool ok = true;
-    for (int j0 = 0; j0 < nj && ok; j0 += 32) {
+    auto fail = [&](int where) {
+      if (!*reinterpret_cast<volatile int*>(dead)) raise_flag(p.status, FLAG_TIMEOUT, where);
+      *reinterpret_cast<volatile int*>(dead) = 1;
+      ok = false;
+    };
+    for (int t0 = 0; t0 < nj + kTqAhead && ok; t0 += 32) {
       int f_n = 0, f_s = 0, f_g = 0, f_b = 0, f_T = 0, f_e0 = 0, f_ph = -1;
-      if (j0 + lane < nj) {
-        const int it = i0 + j0 + lane;
+      if (t0 + lane < nj) {
+        const int it = i0 + t0 + lane;
         const int list = p.item_list[it];
         const int off = p.off[list];
         f_e0 = off + (it - p.item_off[list]) * TPI;
@@ -162,43 +232,59 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
         f_T = bt.seq_len(f_s);
         f_ph = bt.row(f_s)[f_b];
       }
-      for (int t = 0; t < 32 && j0 + t < nj; ++t) {
+      for (int t = 0; t < 32 && t0 + t < nj + kTqAhead; ++t) {
         const int n = __shfl_sync(0xffffffffu, f_n, t), s = __shfl_sync(0xffffffffu, f_s, t);
         const int g = __shfl_sync(0xffffffffu, f_g, t), b = __shfl_sync(0xffffffffu, f_b, t);
         const int T = __shfl_sync(0xffffffffu, f_T, t), e0 = __shfl_sync(0xffffffffu, f_e0, t);
         const int ph = __shfl_sync(0xffffffffu, f_ph, t);
-        const int j = j0 + t;
+        const int jh = t0 + t, jk = jh - kTqAhead;
         if (lane == 0) {
-          const int st = j % kTqStages;
-          if (j >= kTqStages && (*reinterpret_cast<volatile int*>(dead) ||
-                                 !mbar_wait(&kvempty[st], (uint32_t)(((j / kTqStages) - 1) & 1)))) {
-            if (!*reinterpret_cast<volatile int*>(dead)) raise_flag(p.status, FLAG_TIMEOUT, 20);
-            *reinterpret_cast<volatile int*>(dead) = 1;
-            ok = false;
-          } else {
-            uint8_t* sb = base + LY::ST + (size_t)st * LY::STAGE;
-            int32_t* hdr = reinterpret_cast<int32_t*>(sb + LY::S_HDR);
-            const bool okb = ph >= 0 && ph < p.num_blocks && n > 0;
-            if (!okb && n > 0) raise_flag(p.status, FLAG_BAD_BLOCK, ph);
-            const int ea = e0 & ~3, nent = n > 0 ? n : 0;
-            const uint32_t ebytes = (uint32_t)((e0 - ea + nent + 3) & ~3) * 4u;
-            hdr[0] = okb ? n : -nent;  // negative: the block is rejected, its entries get empty partials
-            hdr[1] = s;
-            hdr[2] = g;
-            hdr[3] = b;
-            hdr[4] = T;
-            hdr[5] = e0 - ea;
-            fence_proxy_async();
-            mbar_expect_tx(&kvfull[st], ebytes + (okb ? 2 * kTqTile + 2 * kTqScales : 0u));
-            if (ebytes > 0) bulk_g2s(sb + LY::S_ENT, p.entries + ea, ebytes, &kvfull[st]);
-            if (okb) {
-              const int tile = (int)(((long)ph * G + g) * kBlock);
-              tma_load_2d(sb + LY::S_K, &tmk, 0, tile, &kvfull[st]);
-              tma_load_2d(sb + LY::S_V, &tmv, 0, tile, &kvfull[st]);
-              bulk_g2s(sb + LY::S_KS, p.k_scale + tile, kTqScales, &kvfull[st]);
-              bulk_g2s(sb + LY::S_VS, p.v_scale + tile, kTqScales, &kvfull[st]);
+          if (jh < nj) {  // header jh
+            const int hs = jh % kTqHdrs;
+            if (jh >= kTqHdrs && (*reinterpret_cast<volatile int*>(dead) ||
+                                  !mbar_wait(&hempty[hs], (uint32_t)(((jh / kTqHdrs) - 1) & 1)))) {
+              fail(24);
+            } else {
+              uint8_t* hb = base + LY::HD + (size_t)hs * LY::HSLOT;
+              int32_t* hw = reinterpret_cast<int32_t*>(hb + kTqEnt);
+              const bool okb = ph >= 0 && ph < p.num_blocks && n > 0;
+              if (!okb && n > 0) raise_flag(p.status, FLAG_BAD_BLOCK, ph);
+              const int ea = e0 & ~3, nent = n > 0 ? n : 0;
+              const uint32_t ebytes = (uint32_t)((e0 - ea + nent + 3) & ~3) * 4u;
+              hw[0] = okb ? n : -nent;  // negative: the block is rejected, its entries get empty partials
+              hw[1] = s;
+              hw[2] = g;
+              hw[3] = b;
+              hw[4] = T;
+              hw[5] = e0 - ea;
+              hw[6] = okb ? (int)(((long)ph * G + g) * kBlock) : -1;  // the tile's first row
+              fence_proxy_async();
+              mbar_expect_tx(&hfull[hs], ebytes);
+              if (ebytes > 0) bulk_g2s(hb, p.entries + ea, ebytes, &hfull[hs]);
+              issued_h = jh + 1;
             }
-            issued = j + 1;
+          }
+          if (ok && jk >= 0) {  // tiles of item jk
+            const int st = jk % kTqStages;
+            if (jk >= kTqStages && (*reinterpret_cast<volatile int*>(dead) ||
+                                    !mbar_wait(&kvempty[st], (uint32_t)(((jk / kTqStages) - 1) & 1)))) {
+              fail(20);
+            } else {
+              const int tile = reinterpret_cast<const int32_t*>(base + LY::HD + (size_t)(jk % kTqHdrs) * LY::HSLOT +
+                                                                kTqEnt)[6];
+              uint8_t* sb = base + LY::ST + (size_t)st * LY::STAGE;
+              fence_proxy_async();
+              if (tile >= 0) {
+                mbar_expect_tx(&kvfull[st], 2 * kTqTile + 2 * kTqScales);
+                tma_load_2d(sb + LY::S_K, &tmk, 0, tile, &kvfull[st]);
+                tma_load_2d(sb + LY::S_V, &tmv, 0, tile, &kvfull[st]);
+                bulk_g2s(sb + LY::S_KS, p.k_scale + tile, kTqScales, &kvfull[st]);
+                bulk_g2s(sb + LY::S_VS, p.v_scale + tile, kTqScales, &kvfull[st]);
+              } else {
+                mbar_arrive(&kvfull[st]);  // a rejected block: nothing to copy
+              }
+              issued_k = jk + 1;
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -207,8 +293,12 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
     }
     // a CTA that gave up waits (bounded) for the copies it issued
     if (lane == 0 && !ok) {
-      for (int i = 0; i < kTqStages && i < issued; ++i) {
-        const int jj = issued - 1 - i;
+      for (int i = 0; i < kTqHdrs && i < issued_h; ++i) {
+        const int jj = issued_h - 1 - i;
+        mbar_wait(&hfull[jj % kTqHdrs], (uint32_t)((jj / kTqHdrs) & 1), 2000);
+      }
+      for (int i = 0; i < kTqStages && i < issued_k; ++i) {
+        const int jj = issued_k - 1 - i;
         mbar_wait(&kvfull[jj % kTqStages], (uint32_t)((jj / kTqStages) & 1), 2000);
       }
     }
@@ -225,9 +315,8 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
     const uint32_t lsel = (uint32_t)(32 * quarter) << 16;
     const int terms = p.q_fp8 ? 1 : 2;
     const float qconst = p.q_scale * p.col_const;  // an e4m3 query's row factor
-    uint8_t* ohi = op + (size_t)m * 128;
-    uint8_t* olo = ohi + kTqTile;
-    const int sw = m & 7;
+    const int hh = m & (r - 1);                     // this row's head within the group
+    const uint32_t epitch = (uint32_t)r * 256u + 16u;  // staged output rows: bytes per entry
 
     // every thread of the group waits; the group agrees on the outcome
     auto gwait = [&](uint64_t* bar, uint32_t par, int where) -> bool {
@@ -240,68 +329,71 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
       return !bad;
     };
 
-    // Item j's stage and this thread's row of it, with the row's query loaded
-    // into qv (hi, then lo for a bf16 query) and its factor into rowf.
-    // Rejected items (block outside the cache) get empty partials and release
-    // their stage here; the walk moves on to the group's next item.  Returns
-    // the item taken, or nj.
-    uint4 qv[16];
+    // Item j's header and this thread's row of it; for a real block, the
+    // copies of the row's query into the operand buffer are started (the
+    // warp's 32 rows together: two bf16-split rows of 256 bytes, or four e4m3
+    // rows of 128, per instruction, each chunk straight to its swizzled
+    // place).  Rejected items (block outside the cache) get empty partials and
+    // release their header slot and stage here; the walk moves on to the
+    // group's next item.  Returns the item taken, or nj.
     float rowf_n = 0.f;
     auto take = [&](int j, TqRow& rw) -> int {
       for (; j < nj; j += 2) {
-        const int st = j % kTqStages;
-        if (!gwait(&kvfull[st], (uint32_t)((j / kTqStages) & 1), 21)) return nj;
-        const uint8_t* sb = base + LY::ST + (size_t)st * LY::STAGE;
-        const int32_t* hdr = reinterpret_cast<const int32_t*>(sb + LY::S_HDR);
-        const int n = hdr[0], s = hdr[1], g = hdr[2], b = hdr[3], T = hdr[4], delta = hdr[5];
+        const int hs = j % kTqHdrs;
+        if (!gwait(&hfull[hs], (uint32_t)((j / kTqHdrs) & 1), 21)) return nj;
+        const uint8_t* hb = base + LY::HD + (size_t)hs * LY::HSLOT;
+        const int32_t* hw = reinterpret_cast<const int32_t*>(hb + kTqEnt);
+        const int n = hw[0], s = hw[1], g = hw[2], b = hw[3], T = hw[4], delta = hw[5];
         const int nr = (n < 0 ? -n : n) * r;
-        rw.st = st;
+        rw.hs = hs;
+        rw.st = j % kTqStages;
         rw.valid = m < nr;
         rw.key0 = b * kBlock;
-        const int ent = rw.valid ? reinterpret_cast<const int32_t*>(sb + LY::S_ENT)[delta + (m >> lr)] : 0;
+        const int ent = rw.valid ? reinterpret_cast<const int32_t*>(hb)[delta + (m >> lr)] : 0;
         const long token = ent >> 5;
-        const int head = g * r + (m & (r - 1));
-        rw.part = (token * H + head) * K + (ent & 31);
-        rw.qrow = token * H + head;
+        const int head = g * r + hh;
+        rw.part = (token * K + (ent & 31)) * H + head;
+        rw.qrow = (int)(token * H + head);
         rw.pos = rw.valid ? T - Q + (int)(token - (long)s * Q) : -1;
+        mbar_arrive(&hempty[hs]);  // the header is in registers
         if (n > 0) {
-          if (rw.valid) {
-            if (p.q_fp8) {
-              const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + rw.qrow * 128);
+          uint8_t* wrows = op + (size_t)(32 * quarter) * 128;  // the warp's 32 operand rows
+          if (p.q_fp8) {
 #pragma unroll
-              for (int c = 0; c < 8; ++c) qv[c] = __ldg(src + c);
-              rowf_n = qconst;
-            } else {
-              const uint4* src = reinterpret_cast<const uint4*>(p.qsplit + rw.qrow * 256);
-#pragma unroll
-              for (int c = 0; c < 16; ++c) qv[c] = __ldg(src + c);
-              rowf_n = __ldg(p.qrowf + rw.qrow);
+            for (int i = 0; i < 8; ++i) {
+              const int rho = 4 * i + (lane >> 3), c = lane & 7;
+              const int qr = __shfl_sync(0xffffffffu, rw.qrow, rho);
+              const int vd = __shfl_sync(0xffffffffu, rw.valid, rho);
+              cp_async16(wrows + rho * 128 + ((c ^ (rho & 7)) << 4),
+                         static_cast<const uint8_t*>(p.q) + (long)(vd ? qr : 0) * 128 + 16 * c, vd != 0);
             }
+            rowf_n = rw.valid ? qconst : 0.f;
           } else {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) qv[c] = make_uint4(0u, 0u, 0u, 0u);
-            rowf_n = 0.f;
+            for (int i = 0; i < 16; ++i) {
+              const int rho = 2 * i + (lane >> 4), c = lane & 15;
+              const int qr = __shfl_sync(0xffffffffu, rw.qrow, rho);
+              const int vd = __shfl_sync(0xffffffffu, rw.valid, rho);
+              cp_async16(wrows + (c >> 3) * kTqTile + rho * 128 + (((c & 7) ^ (rho & 7)) << 4),
+                         p.qsplit + (long)(vd ? qr : 0) * 256 + 16 * c, vd != 0);
+            }
+            rowf_n = rw.valid ? __ldg(p.qrowf + rw.qrow) : 0.f;
           }
+          cp_async_commit();
           return j;
         }
         if (rw.valid) reinterpret_cast<float4*>(p.part_ml)[rw.part] = make_float4(-INFINITY, 0.f, 1.f, 0.f);
-        named_bar_sync(bar_id, 128);  // every row has read the stage
-        if (leader) mbar_arrive(&kvempty[st]);
+        mbar_arrive(&kvempty[rw.st]);  // no tiles to read: the stage goes straight back
       }
       return nj;
     };
 
-    // the loaded query rows into the operand (swizzled K-major rows), then MMA 1
-    auto start = [&](const TqRow& rw) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(ohi + ((c ^ sw) << 4)) = qv[c];
-      if (terms == 2) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(olo + ((c ^ sw) << 4)) = qv[8 + c];
-      }
+    // the query operand is in place and the item's tiles are in: MMA 1
+    auto start = [&](const TqRow& rw, int j) -> bool {
+      cp_async_wait();
       fence_proxy_async();  // the MMA reads the operand through the async proxy
       tc_fence_before();
-      named_bar_sync(bar_id, 128);
+      if (!gwait(&kvfull[rw.st], (uint32_t)((j / kTqStages) & 1), 25)) return false;
       if (leader) {
         tc_fence_after();
         const uint32_t kt = smem_u32(base + LY::ST + (size_t)rw.st * LY::STAGE + LY::S_K);
@@ -313,28 +405,30 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
                    (term | k) != 0);
         mma_commit(&sbar[grp]);
       }
+      return true;
     };
 
     TqRow cur, nxt;
     int u = 0;  // items of this group whose MMAs ran (phases of sbar / obar)
     int j = take(grp, cur);
     float rowf = rowf_n;
-    if (j < nj) start(cur);
+    if (j < nj && !start(cur, j)) j = nj;
 #pragma unroll 1
     while (j < nj) {
       if (!gwait(&sbar[grp], (uint32_t)(u & 1), 22)) break;
       tc_fence_after();
+      // MMA 1 is done with the operand buffer: the next item's query rows go in
+      const int jn = take(j + 2, nxt);
       const uint8_t* sb = base + LY::ST + (size_t)cur.st * LY::STAGE;
       const float* ks = reinterpret_cast<const float*>(sb + LY::S_KS);
       const float* vs = reinterpret_cast<const float*>(sb + LY::S_VS);
-      // P's scale 2^e puts the block's largest V scale at most at 448; the
-      // fp16 partial o / l (at most max |v| <= 448 x that scale) is brought
-      // under 32768 by 2^-ev
+      // P's scale 2^e puts the block's largest V scale at most at 448 (2^e at
+      // most 2^100, so that l cannot overflow); the fp16 partial o / l, at most
+      // max |v| <= 448 x that scale, is brought under 32768 by 2^-ev
       float vmx = fmaxf(fmaxf(vs[lane], vs[lane + 32]), fmaxf(vs[lane + 64], vs[lane + 96]));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, o));
-      const int e = min(126, fit448(vmx));
-      const float fe = (e >= -126) ? pow2i(e) : ldexpf(1.f, e);
+      const int e = min(100, fit448(vmx));
       int ev = 0;
       if (448.f * vmx > 32768.f) frexpf(448.f * vmx * (1.f / 32768.f), &ev);
       const bool full = cur.key0 + kBlock - 1 <= cur.pos;  // every key visible
@@ -342,130 +436,135 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
       float mx = -INFINITY;
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
-        float v[1][32];
-        tmem_ld32(tS + lsel + 32 * h, v[0]);
+        float v[32];
+        tmem_ld32(tS + lsel + 32 * h, v);
         tmem_ld_wait();
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        {
-          constexpr int q = 0;
-          const int n0 = 32 * h;
-          if (full) {
-            const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
+        const int n0 = 32 * h;
+        if (full) {
+          const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
 #pragma unroll
-            for (int n = 0; n < 32; n += 8) {
-              const float4 ka = k4[n >> 2], kb = k4[(n >> 2) + 1];
-              const float2 p0 = mul2(v[q][n], v[q][n + 1], ka.x, ka.y);
-              const float2 p1 = mul2(v[q][n + 2], v[q][n + 3], ka.z, ka.w);
-              const float2 p2 = mul2(v[q][n + 4], v[q][n + 5], kb.x, kb.y);
-              const float2 p3 = mul2(v[q][n + 6], v[q][n + 7], kb.z, kb.w);
-              m4[0] = max3(m4[0], p0.x, p0.y);
-              m4[1] = max3(m4[1], p1.x, p1.y);
-              m4[2] = max3(m4[2], p2.x, p2.y);
-              m4[3] = max3(m4[3], p3.x, p3.y);
-            }
-          } else {
+          for (int n = 0; n < 32; n += 8) {
+            const float4 ka = k4[n >> 2], kb = k4[(n >> 2) + 1];
+            const float2 p0 = mul2(v[n], v[n + 1], ka.x, ka.y);
+            const float2 p1 = mul2(v[n + 2], v[n + 3], ka.z, ka.w);
+            const float2 p2 = mul2(v[n + 4], v[n + 5], kb.x, kb.y);
+            const float2 p3 = mul2(v[n + 6], v[n + 7], kb.z, kb.w);
+            m4[0] = max3(m4[0], p0.x, p0.y);
+            m4[1] = max3(m4[1], p1.x, p1.y);
+            m4[2] = max3(m4[2], p2.x, p2.y);
+            m4[3] = max3(m4[3], p3.x, p3.y);
+          }
+        } else {
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-              const float sc = (cur.key0 + n0 + n <= cur.pos) ? v[q][n] * ks[n0 + n] : -INFINITY;
-              m4[n & 3] = fmaxf(m4[n & 3], sc);
-            }
+          for (int n = 0; n < 32; ++n) {
+            const float sc = (cur.key0 + n0 + n <= cur.pos) ? v[n] * ks[n0 + n] : -INFINITY;
+            m4[n & 3] = fmaxf(m4[n & 3], sc);
           }
         }
         mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
       }
-      const float m2 = mx * rowf;                           // base-2 logit maximum (rowf > 0)
-      const float msub = (mx == -INFINITY) ? 0.f : m2;
-      // ---- p_t = 2^(x_t - m), l = sum p_t, P'_t = p_t vscale_t 2^e as e4m3 hi + lo
+      const float m2 = mx * rowf;  // base-2 logit maximum (rowf > 0)
+      // p_t 2^e = 2^(x_t - m + e): the exponent's offset, -inf rows kept at 0
+      const float c0 = (mx == -INFINITY) ? 0.f : (float)e - m2;
+      // ---- P'_t = p_t 2^e vscale_t as e4m3 hi + lo into the S columns read
+      // (chunk h of 32 keys: hi at column 16h, lo at 16h + 8), l 2^e = sum p_t 2^e
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
-        float v[1][32];
-        tmem_ld32(tS + lsel + 32 * h, v[0]);
+        float v[32];
+        tmem_ld32(tS + lsel + 32 * h, v);
         tmem_ld_wait();
-        constexpr int q = 0;
+        const int n0 = 32 * h;
+        uint32_t hw[8], lw[8];
 #pragma unroll
-          for (int c16 = 0; c16 < 2; ++c16) {
-            const int n0 = 32 * h + 16 * c16;  // first key of this 16-key chunk
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int n = n0 + 2 * i;
-              const float2 t = mul2(v[q][16 * c16 + 2 * i], v[q][16 * c16 + 2 * i + 1], ks[n], ks[n + 1]);
-              float x0 = fmaf(t.x, rowf, -msub), x1 = fmaf(t.y, rowf, -msub);
-              if (!full) {
-                if (cur.key0 + n > cur.pos) x0 = -INFINITY;
-                if (cur.key0 + n + 1 > cur.pos) x1 = -INFINITY;
-              }
-              const float p0 = tq_ex2(x0), p1 = tq_ex2(x1);
-              l0 += p0;
-              l1 += p1;
-              const float2 vf = mul2(vs[n], vs[n + 1], fe, fe);
-              const float2 pp = mul2(p0, p1, vf.x, vf.y);
-              const uint16_t hb = pack_e4m3x2(pp.x, pp.y);
-              const float2 hv = e4m3x2_to_float2(hb);
-              const uint16_t lb = pack_e4m3x2(pp.x - hv.x, pp.y - hv.y);
-              if (i & 1) {
-                hw[i >> 1] |= (uint32_t)hb << 16;
-                lw[i >> 1] |= (uint32_t)lb << 16;
-              } else {
-                hw[i >> 1] = hb;
-                lw[i >> 1] = lb;
-              }
-            }
-            const int c = n0 >> 4;  // 16-byte chunk of the 128-key row
-            *reinterpret_cast<uint4*>(ohi + ((c ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(olo + ((c ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        for (int q4 = 0; q4 < 8; ++q4) {  // keys n0 + 4 q4 .. + 3: one word of each term
+          const int n = n0 + 4 * q4;
+          const float4 k4 = *reinterpret_cast<const float4*>(ks + n);
+          const float4 v4 = *reinterpret_cast<const float4*>(vs + n);
+          const float2 ta = mul2(v[4 * q4], v[4 * q4 + 1], k4.x, k4.y);
+          const float2 tb = mul2(v[4 * q4 + 2], v[4 * q4 + 3], k4.z, k4.w);
+          float x0 = fmaf(ta.x, rowf, c0), x1 = fmaf(ta.y, rowf, c0);
+          float x2 = fmaf(tb.x, rowf, c0), x3 = fmaf(tb.y, rowf, c0);
+          if (!full) {
+            if (cur.key0 + n > cur.pos) x0 = -INFINITY;
+            if (cur.key0 + n + 1 > cur.pos) x1 = -INFINITY;
+            if (cur.key0 + n + 2 > cur.pos) x2 = -INFINITY;
+            if (cur.key0 + n + 3 > cur.pos) x3 = -INFINITY;
           }
+          const float p0 = tq_ex2(x0), p1 = tq_ex2(x1), p2 = tq_ex2(x2), p3 = tq_ex2(x3);
+          l0 += p0 + p2;
+          l1 += p1 + p3;
+          const float2 pa = mul2(p0, p1, v4.x, v4.y);
+          const float2 pb = mul2(p2, p3, v4.z, v4.w);
+          uint32_t ha, la, hb, lb;
+          split2_e4m3(pa.x, pa.y, ha, la);
+          split2_e4m3(pb.x, pb.y, hb, lb);
+          hw[q4] = ha | (hb << 16);
+          lw[q4] = la | (lb << 16);
+        }
+        tmem_st8(tS + lsel + 16 * h, hw);
+        tmem_st8(tS + lsel + 16 * h + 8, lw);
       }
-      const float l = l0 + l1;
-      fence_proxy_async();
+      const float le = l0 + l1;  // l x 2^e
+      tmem_st_wait();
       tc_fence_before();
       named_bar_sync(bar_id, 128);
       if (leader) {
         tc_fence_after();
         const uint32_t vt = smem_u32(sb + LY::S_V);
 #pragma unroll
-        for (int term = 0; term < 2; ++term)
+        for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f8(tO, sw128_desc(op_s + term * kTqTile + 32 * k), sw128_desc_mn(vt + 4096 * k), kIdescPV,
-                   (term | k) != 0);
+          for (int term = 0; term < 2; ++term)
+            mma_f8_ts(tO, tS + 16 * kk + 8 * term, sw128_desc_mn(vt + 4096 * kk), kIdescPV, (term | kk) != 0);
         mma_commit(&obar[grp]);
-        mma_commit(&kvempty[cur.st]);  // the stage is free once MMA 2 has read V
       }
-      // the group's next item: its stage and query rows, while MMA 2 runs
-      const int jn = take(j + 2, nxt);
       if (!gwait(&obar[grp], (uint32_t)(u & 1), 23)) break;
       tc_fence_after();
       ++u;
-      if (jn < nj) start(nxt);  // MMA 1 of the next item overlaps this item's output
-      // ---- o / l x 2^-ev as fp16, with (m, l, 2^ev)
-      const float inv = l > 0.f ? ldexpf(__frcp_rn(l), -e - ev) : 0.f;
-      __half* dst = reinterpret_cast<__half*>(p.part_o) + cur.part * 128;
+      // P has been read: the next item's MMA 1 overlaps this item's output
+      if (jn < nj && !start(nxt, jn)) break;
+      // ---- o / l x 2^-ev as fp16 rows, staged entry by entry in this item's
+      // stage (its tiles, scales and header are no longer read), one bulk copy
+      // per entry; then (m, l, 2^ev); the stage goes back to the producer once
+      // the copies have read it
+      const float inv = le > 0.f ? ldexpf(__frcp_rn(le), -ev) : 0.f;
+      uint8_t* orow = base + LY::ST + (size_t)cur.st * LY::STAGE + (size_t)(m >> lr) * epitch + (size_t)hh * 256;
 #pragma unroll 1
       for (int h = 0; h < 4; ++h) {
-        float v[1][32];
-        tmem_ld32(tO + lsel + 32 * h, v[0]);
+        float v[32];
+        tmem_ld32(tO + lsel + 32 * h, v);
         tmem_ld_wait();
-        if (cur.valid) {
-          constexpr int q = 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint4 w;
-              w.x = pack_f16x2(v[q][8 * c] * inv, v[q][8 * c + 1] * inv);
-              w.y = pack_f16x2(v[q][8 * c + 2] * inv, v[q][8 * c + 3] * inv);
-              w.z = pack_f16x2(v[q][8 * c + 4] * inv, v[q][8 * c + 5] * inv);
-              w.w = pack_f16x2(v[q][8 * c + 6] * inv, v[q][8 * c + 7] * inv);
-              *reinterpret_cast<uint4*>(dst + 32 * h + 8 * c) = w;
-            }
+        for (int c = 0; c < 4; ++c) {
+          uint4 w;
+          w.x = pack_f16x2(v[8 * c] * inv, v[8 * c + 1] * inv);
+          w.y = pack_f16x2(v[8 * c + 2] * inv, v[8 * c + 3] * inv);
+          w.z = pack_f16x2(v[8 * c + 4] * inv, v[8 * c + 5] * inv);
+          w.w = pack_f16x2(v[8 * c + 6] * inv, v[8 * c + 7] * inv);
+          *reinterpret_cast<uint4*>(orow + 64 * h + 16 * c) = w;
         }
       }
-      if (cur.valid) reinterpret_cast<float4*>(p.part_ml)[cur.part] = make_float4(m2, l, ldexpf(1.f, ev), 0.f);
+      // the rows written here are read next by the bulk copies (and later
+      // overwritten by the producer's copies): order them for the async proxy
+      fence_proxy_async();
+      __syncwarp();  // an entry's r rows are written by r lanes of one warp
+      if (cur.valid && hh == 0) {
+        bulk_s2g(reinterpret_cast<__half*>(p.part_o) + cur.part * 128, orow, (uint32_t)r * 256u);
+        bulk_commit();
+      }
+      if (cur.valid)
+        reinterpret_cast<float4*>(p.part_ml)[cur.part] = make_float4(m2, ldexpf(le, -e), ldexpf(1.f, ev), 0.f);
+      bulk_wait_read();
+      mbar_arrive(&kvempty[cur.st]);
       tc_fence_before();  // the O reads come before the next MMA 2 (ordered by the group's next barrier)
       j = jn;
       cur = nxt;
       rowf = rowf_n;
     }
+    cp_async_wait();
+    bulk_wait_all();
     // every MMA this leader issued has completed before TMEM is freed
     if (leader) {
       mma_commit(&done[grp]);
