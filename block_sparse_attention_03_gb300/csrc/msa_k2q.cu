@@ -135,13 +135,17 @@ __device__ __forceinline__ float k2q_ex2(float x) {
   return y;
 }
 
-// One warp per (token, head): lane l holds dims 4l .. 4l+3; the token's
-// selected slots merged by log-sum-exp in base 2 (m and l come that way).
+// One warp per (token, head): the token's selected slots merged by
+// log-sum-exp in base 2 (m and l come that way).  Every load of the row is
+// issued at once: lane k < topk takes slot k's (m, l, 2^ev), and the two
+// half-warps take the even and the odd slots' o / l rows, lane l holding dims
+// 8 (l % 16) .. + 7 with one 16-byte load a slot (32 slots at most).
+template <int KMAX>
 __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
   const int H = p.G * p.r;
   const long rows = (long)bt.S * bt.Q * H;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, half = lane >> 4, d8 = 8 * (lane & 15);
   const long nw = (long)gridDim.x * (blockDim.x >> 5);
   for (long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
     const long token = row / H;
@@ -152,8 +156,13 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const int s = (int)(token / bt.Q), i = (int)(token % bt.Q);
     const int T = bt.seq_len(s);
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
-    // lane k < topk: slot k's (m, l); the row's max M and weights w_k = l_k 2^(m_k - M)
-    // by warp reductions, then every slot's o / l loaded independently
+    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + (token * p.topk * H + h) * 128 + d8);
+    uint4 ov[KMAX / 2];
+#pragma unroll
+    for (int q = 0; q < KMAX / 2; ++q) {  // slot 2q + half
+      const int k = 2 * q + half;
+      ov[q] = k < p.topk ? __ldcg(orow + (long)k * H * 16) : make_uint4(0u, 0u, 0u, 0u);
+    }
     float mk = -INFINITY, lk = 0.f, fk = 1.f;
     const int bl = lane < p.topk ? sel[lane] : -1;
     // a block an earlier slot already names has no list entry (k2q_list)
@@ -161,9 +170,8 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     if (lane < p.topk) {
       const int b = bl;
       if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
-        const long part = (token * p.topk + lane) * H + h;
-        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + part);  // m, l, 2^ev
-        mk = ml.x;
+        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + (token * p.topk + lane) * H + h);
+        mk = ml.x;  // m, l, 2^ev
         lk = ml.y;
         fk = ml.z;
       }
@@ -176,26 +184,31 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     float Lsum = wk;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int k = 0; k < p.topk; ++k) {
-      const float w = __shfl_sync(0xffffffffu, wo, k);
-      if (w == 0.f) continue;  // warp-uniform
-      const uint2 pk = __ldcg(reinterpret_cast<const uint2*>(p.part_o + ((token * p.topk + k) * H + h) * 128) + lane);
-      const float2 o01 = __half22float2(*reinterpret_cast<const __half2*>(&pk.x));
-      const float2 o23 = __half22float2(*reinterpret_cast<const __half2*>(&pk.y));
-      acc.x += w * o01.x;
-      acc.y += w * o01.y;
-      acc.z += w * o23.x;
-      acc.w += w * o23.y;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < KMAX / 2; ++q) {
+      const float w = __shfl_sync(0xffffffffu, wo, 2 * q + half);
+      if (w != 0.f) {  // a slot left out may hold anything: select, do not multiply
+        const __half2* hv = reinterpret_cast<const __half2*>(&ov[q]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = __half22float2(hv[t]);
+          acc[2 * t] += w * f.x;
+          acc[2 * t + 1] += w * f.y;
+        }
+      }
     }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
     const float inv = Lsum > 0.f ? __fdividef(1.f, Lsum) : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * 128 + 4 * lane) = pk;
+    if (half == 0) {
+      uint4 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * 128 + d8) = pk;
+    }
     if (lane == 0 && p.lse) p.lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
   }
 }
@@ -221,7 +234,8 @@ cudaError_t launch_k2q_combine(const K2qParams& p, cudaStream_t st) {
   long grid = (rows + 7) / 8;
   if (grid > 65535) grid = 65535;
   if (grid < 1) grid = 1;
-  k2q_combine_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
+  if (p.topk <= 16) k2q_combine_kernel<16><<<(unsigned)grid, 256, 0, st>>>(p);
+  else k2q_combine_kernel<32><<<(unsigned)grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
