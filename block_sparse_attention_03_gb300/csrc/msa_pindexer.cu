@@ -17,7 +17,7 @@
 // e4m3 hi + lo terms that accumulate into the same TMEM columns, carrying all 8
 // significant bits of bf16; an e4m3 index query enters as is.
 //
-// One CTA (10 warps, persistent, one per SM) walks a contiguous run of units
+// One CTA (18 warps, persistent, one per SM) walks a contiguous run of units
 // (query tile, two key blocks):
 //   warp 0   copies key tiles (TMA, 128-byte swizzle) into a 5-stage ring of
 //            two-tile stages (enough bytes in flight to cover L2 latency at the
@@ -25,12 +25,15 @@
 //            scales into a 16-slot ring freed by the epilogue;
 //   warp 1   owns the SM's 512 TMEM columns (two 256-column accumulators); one
 //            thread issues the MMAs and commits them to mbarriers;
-//   warps 2-9 two groups of four, taking alternate units; each thread owns one
-//            accumulator row (tcgen05.ld 32x32b), multiplies by the key scales
+//   warps 2-17 four groups of four: groups 0 and 1 take the even units, 2 and
+//            3 the odd ones, each pair one key block of the unit apiece (twice
+//            the warps of one group per row, to hide the TMEM-load and
+//            arithmetic latency); each thread owns one accumulator row
+//            (tcgen05.ld 32x32b) of its block, multiplies by the key scales
 //            (packed f32x2), masks the keys its token cannot see, takes the max
-//            (three-input max) and writes P.  At each new query tile both
-//            groups build its operand (hi / lo e4m3 in the swizzled K-major
-//            layout the MMA reads), group 0 the hi term, group 1 the lo term.
+//            (three-input max) and writes P.  At each new query tile groups 0
+//            and 2 build its operand (hi / lo e4m3 in the swizzled K-major
+//            layout the MMA reads), group 0 the hi term, group 2 the lo term.
 // Every mbarrier wait is bounded; a wait that gives up sets the timeout flag,
 // the CTA stops issuing, drains what it issued and frees its TMEM.
 #include "msa_device.cuh"
@@ -45,7 +48,7 @@ constexpr int kPiStages = 5;                   // units (two key tiles) in fligh
 constexpr int kPiSStages = 16;                 // key-scale slots (released by the epilogue, which lags)
 constexpr int kPiAcc = 2;                      // accumulators of 256 columns (two key blocks)
 constexpr int kPiCols = 256 * kPiAcc;          // TMEM columns (all 512 of the SM: one CTA per SM)
-constexpr int kPiThreads = 320;                // producer, MMA, 2 x 4 epilogue warps
+constexpr int kPiThreads = 576;                // producer, MMA, 4 x 4 epilogue warps
 constexpr uint32_t kPiTile = 128 * 128;        // bytes of one e4m3 128 x 128 tile
 constexpr uint32_t kPiStage = 2 * kPiTile;     // a unit's two key tiles, one 256-row operand
 constexpr uint32_t kPiScales = 128 * 4;        // fp32 key scales of one block
@@ -170,11 +173,11 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
     }
     for (int i = 0; i < kPiSStages; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 4);  // the unit's four epilogue warps
+      mbar_init(&sempty[i], 8);  // the unit's eight epilogue warps
     }
     for (int i = 0; i < kPiAcc; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 8);
     }
     mbar_init(afull, 8);
     mbar_init(aempty, 1);
@@ -292,7 +295,10 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
   } else {
     // ---------------- query tiles + epilogue (thread = accumulator row)
     const int quarter = warp & 3;          // TMEM lanes 32 * quarter .. + 31
-    const int group = (warp - 2) >> 2;     // takes the units j with j % 2 == group
+    const int egrp = (warp - 2) >> 2;      // 0..3
+    const int group = egrp >> 1;           // takes the units j with j % 2 == group
+    const int hb = egrp & 1;               // and key block hb of each
+    const bool builder = hb == 0;          // groups 0 and 2 build the query operand (hi / lo)
     const int m = 32 * quarter + lane;     // row of the tile: token m / G, group m % G
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     UnitCursor c;
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         if (p.iq_fp8) {
           const uint8_t* src = static_cast<const uint8_t*>(p.index_q) + qoff;
 #pragma unroll
-          for (int ch = 0; ch < 8 && group == 0; ++ch) {
+          for (int ch = 0; ch < 8 && builder && group == 0; ++ch) {
             const uint4 v = row_ok ? *reinterpret_cast<const uint4*>(src + 16 * ch) : make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(ahi + ((ch ^ (m & 7)) << 4)) = v;
           }
@@ -358,13 +364,16 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
                 lw[2 * half + e / 2] = (uint32_t)pack_e4m3x2(l0, l1) | ((uint32_t)pack_e4m3x2(l2, l3) << 16);
               }
             }
+            if (!builder) continue;
             if (group == 0) *reinterpret_cast<uint4*>(ahi + ((ch ^ (m & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             else *reinterpret_cast<uint4*>(alo + ((ch ^ (m & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
-        fence_proxy_async();  // the MMA reads the operand through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(afull);
+        if (builder) {
+          fence_proxy_async();  // the MMA reads the operand through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(afull);
+        }
         ++a_use;
       }
       if ((j & 1) != group) {  // the other group's unit
@@ -374,8 +383,8 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
       const int ab = j % kPiAcc;
       const int nblocks = (2 * c.b + 1 < c.nblk) ? 2 : 1;  // the unit's key blocks
       // physical blocks, used at the end: their latency hides behind the waits
-      const int ph0 = bt.row(c.s)[2 * c.b];
-      const int ph1 = nblocks == 2 ? bt.row(c.s)[2 * c.b + 1] : -1;
+      const int ph0 = hb == 0 ? bt.row(c.s)[2 * c.b] : -1;
+      const int ph1 = (hb == 1 && nblocks == 2) ? bt.row(c.s)[2 * c.b + 1] : -1;
       if (!pi_wait(&tfull[ab], (uint32_t)((j / kPiAcc) & 1), dead, p.status, 6)) break;
       // the unit's key scales (their own ring: the slot is not reused before
       // this group releases it)
@@ -384,22 +393,21 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
       tc_fence_after();
       float mxs[2] = {-INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int h = 0; h < nblocks; ++h) {  // warp-uniform: the unit is the same for the whole warp
+      for (int h = hb; h < nblocks && h == hb; ++h) {  // this group's block of the unit, if it has one
         const float* ks = reinterpret_cast<const float*>(base + LY::KS + (size_t)ss * kPiSSlot) + 128 * h;
         const int key0 = (2 * c.b + h) * kBlock;
         const bool full_vis = key0 + kBlock - 1 <= pos;
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {  // 64 columns: two loads in flight, one wait
-          float v[2][32];
-          const uint32_t col = (uint32_t)(ab * 256 + 128 * h + 64 * half);
+        for (int half = 0; half < 4; ++half) {  // 32 columns a load (more warps hide the wait)
+          float v[1][32];
+          const uint32_t col = (uint32_t)(ab * 256 + 128 * h + 32 * half);
           tmem_ld32(lane_addr + col, v[0]);
-          tmem_ld32(lane_addr + col + 32, v[1]);
           tmem_ld_wait();
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int n0 = 64 * half + 32 * q;
+          for (int q = 0; q < 1; ++q) {
+            const int n0 = 32 * half;
             if (full_vis) {
               const float4* k4 = reinterpret_cast<const float4*>(ks + n0);
 #pragma unroll
@@ -432,10 +440,9 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         mbar_arrive(&tempty[ab]);  // the accumulator may be overwritten
         mbar_arrive(&sempty[ss]);  // done with the scales
       }
-      if (row_ok) {
-        prow[2 * c.b] = (ph0 >= 0 && ph0 < p.num_blocks) ? mxs[0] * rowf : -INFINITY;
-        if (nblocks == 2) prow[2 * c.b + 1] = (ph1 >= 0 && ph1 < p.num_blocks) ? mxs[1] * rowf : -INFINITY;
-      }
+      if (row_ok && hb == 0) prow[2 * c.b] = (ph0 >= 0 && ph0 < p.num_blocks) ? mxs[0] * rowf : -INFINITY;
+      if (row_ok && hb == 1 && nblocks == 2)
+        prow[2 * c.b + 1] = (ph1 >= 0 && ph1 < p.num_blocks) ? mxs[1] * rowf : -INFINITY;
       pi_advance(bt, tiles, c);
     }
   }
