@@ -45,7 +45,8 @@ class MsaCacheT(ctypes.Structure):
                 ("k_sf", ctypes.c_void_p), ("v_sf", ctypes.c_void_p),
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("idx", ctypes.c_void_p), ("idx_sf", ctypes.c_void_p), ("idx_scale", ctypes.c_void_p),
-                ("k_global", ctypes.c_float), ("v_global", ctypes.c_float), ("idx_global", ctypes.c_float)]
+                ("k_global", ctypes.c_float), ("v_global", ctypes.c_float), ("idx_global", ctypes.c_float),
+                ("nvfp4_mode", ctypes.c_int32)]
 
 
 class MsaBatchT(ctypes.Structure):
@@ -60,7 +61,9 @@ class MsaConfigT(ctypes.Structure):
                 ("sm_scale", ctypes.c_float), ("score_type", ctypes.c_int32)]
 
 
-SCORE_TYPES = {"max": 0}  # msa_score_type_t: the block pooling of the index scores
+SCORE_TYPES = {"max": 0}
+# msa_nvfp4_mode_t: "exact" e2m1 x e4m3 products, or "e4m3": rounded to E4M3 first
+NVFP4_MODES = {"exact": 0, "e4m3": 1}  # msa_score_type_t: the block pooling of the index scores
 
 
 class MsaQueryT(ctypes.Structure):
@@ -138,13 +141,15 @@ class PagedCache:
     idx_global: float = 0.0
     head_dim: int = 128
     index_dim: int = 128
+    nvfp4_mode: str = "exact"
 
     def struct(self) -> MsaCacheT:
         return MsaCacheT(DTYPES[self.kv_dtype], DTYPES[self.index_dtype], self.num_blocks, 128,
                          self.num_kv_heads, self.head_dim, self.index_dim,
                          _ptr(self.k), _ptr(self.v), _ptr(self.k_sf), _ptr(self.v_sf),
                          _ptr(self.k_scale), _ptr(self.v_scale), _ptr(self.idx), _ptr(self.idx_sf),
-                         _ptr(self.idx_scale), self.k_global, self.v_global, self.idx_global)
+                         _ptr(self.idx_scale), self.k_global, self.v_global, self.idx_global,
+                         NVFP4_MODES.get(self.nvfp4_mode, -1))
 
 
 @dataclasses.dataclass

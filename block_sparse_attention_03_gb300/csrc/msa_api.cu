@@ -98,6 +98,7 @@ msa_status_t check_cfg(const msa_config_t* c) {
 }
 
 msa_status_t check_cache(const msa_cache_t* c, bool need_index, bool need_kv) {
+  if (c && c->nvfp4_mode != MSA_NVFP4_EXACT && c->nvfp4_mode != MSA_NVFP4_E4M3_PRODUCT) return MSA_ERR_INVALID_ARGUMENT;
   if (!c) return MSA_ERR_INVALID_ARGUMENT;
   if (c->block_size != kBlock || c->head_dim != kDim || c->index_dim != kDim) return MSA_ERR_UNSUPPORTED;
   if (c->num_kv_heads < 1 || c->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
@@ -303,6 +304,7 @@ msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_c
   ip.iq_fp8 = iq->dtype == MSA_DTYPE_FP8_E4M3;
   ip.iq_scale = ip.iq_fp8 ? iq->scale : 1.f;
   ip.col_const = cfg->index_scale * (fi == FMT_NVFP4 ? c->idx_global : 1.f);
+  ip.nv_round = c->nvfp4_mode == MSA_NVFP4_E4M3_PRODUCT ? 1 : 0;
   ip.geom = pl.gi;
   ip.pooled = pooled;
   ip.status = at<DeviceStatus>(ws, pl.off_status);
@@ -410,6 +412,7 @@ msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_co
   ap.k_scale = c->k_scale;
   ap.v_scale = c->v_scale;
   ap.v_global = c->v_global;
+  ap.nv_round = c->nvfp4_mode == MSA_NVFP4_E4M3_PRODUCT ? 1 : 0;
   ap.q = q->data;
   ap.q_fp8 = q->dtype == MSA_DTYPE_FP8_E4M3;
   ap.q_scale = ap.q_fp8 ? q->scale : 1.f;

@@ -162,7 +162,8 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
                                              const uint32_t* __restrict__ fr, int ct, const float (&colf)[2],
                                              const int (&qlim)[2], const int (&qbit)[2], uint32_t qmask, int key0,
                                              int kw, int warp, int lane, float (&m_run)[2], float (&l_run)[2],
-                                             float (&o)[8][4], int& e_prev, unsigned phases = kAllPhases) {
+                                             float (&o)[8][4], int& e_prev, unsigned phases = kAllPhases,
+                                             bool nvr = false) {
   using TR = AttTraits<FMT>;
   constexpr int MT = 2 * NT;  // m tiles of 16 keys
   constexpr int KW = 16 * MT; // keys of this warp
@@ -235,6 +236,10 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
         a[2] = *reinterpret_cast<uint32_t*>(&t);
         t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[grp]));
         a[3] = *reinterpret_cast<uint32_t*>(&t);
+        if (nvr) {  // the product rounded to E4M3, as the Blackwell NVFP4 -> FP8 dequant does
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a[q] = e4m3_round_f16x2(a[q]);
+        }
         mma_f16_k16(sacc[mt], a, QF(0, ks, 0), QF(0, ks, 1));
       }
     }
@@ -394,6 +399,7 @@ __device__ __forceinline__ void attend_block(const uint8_t* stg, uint8_t* psm, u
           uint32_t x = e2m1x2_to_f16x2((ww[bi >> 2] >> (8 * (bi & 3))) & 0xffu);
           __half2 t = __hmul2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<const __half2*>(bi < 8 ? &sA : &sB));
           out[bi] = *reinterpret_cast<uint32_t*>(&t);
+          if (nvr) out[bi] = e4m3_round_f16x2(out[bi]);
         }
         // 32 dims = d 32*q4 .. +31 -> f16 bytes 64*q4 .. +63 -> half (q4>>1), chunks 4*(q4&1) .. +3
 #pragma unroll
@@ -824,7 +830,7 @@ __device__ __forceinline__ void attend_consumer(const AttendParams& p, uint8_t* 
       if (have && (dry || f.sok[k])) {
         attend_block<FMT, NT, SP>(base + (size_t)st * LY::STAGE, psm, vdq, fr, ct, colf, qlim, qbit,
                                   dry ? 0u : f.smask[k], (dry ? 0 : f.sb[k]) * kBlock + kw, kw, warp, lane, m_run,
-                                  l_run, o, e_prev, dry ? (1u << warp) : kAllPhases);
+                                  l_run, o, e_prev, dry ? (1u << warp) : kAllPhases, p.nv_round != 0);
       }
       __syncwarp();
       if (!dry && lane == 0) mbar_arrive(&empty[st]);

@@ -5,7 +5,10 @@
 //   BF16   the bits widened to fp32 (exact);
 //   FP8    fp32(e4m3) * per-token fp32 scale, one round-to-nearest-even;
 //   NVFP4  fp32(e2m1 * e4m3 block scale) * fp32 per-tensor scale; the inner
-//          product is exact, so again one rounding.
+//          product is exact, so again one rounding.  With the cache's
+//          MSA_NVFP4_E4M3_PRODUCT mode the product is first rounded to E4M3
+//          (nearest even, saturating), as the Blackwell kernels' dequant does
+//          ("NVIDIA Blackwell 优化的 MSA 内核").
 #include "msa_device.cuh"
 #include "msa_internal.h"
 
@@ -50,7 +53,8 @@ __global__ void dequant_kernel(int fmt, int which, msa_cache_t c, const int32_t*
       const uint8_t* sfp = static_cast<const uint8_t*>(is_idx ? c.idx_sf : (which == 0 ? c.k_sf : c.v_sf));
       const uint8_t sfc = sfp[row * (D / 16) + d / 16];
       const float gl = is_idx ? c.idx_global : (which == 0 ? c.k_global : c.v_global);
-      const float prod = __fmul_rn(e2m1_to_float((d & 1) ? (byte >> 4) : (byte & 0xf)), e4m3_to_float(sfc));
+      float prod = __fmul_rn(e2m1_to_float((d & 1) ? (byte >> 4) : (byte & 0xf)), e4m3_to_float(sfc));
+      if (c.nvfp4_mode == MSA_NVFP4_E4M3_PRODUCT) prod = e4m3_to_float((uint8_t)(pack_e4m3x2(prod, 0.f) & 0xffu));
       v = __fmul_rn(prod, gl);
     }
     out[e] = v;

@@ -225,6 +225,14 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return h;
 }
 
+// Two f16 values rounded to E4M3 (nearest, ties to even, saturating at
+// +-448) and widened back to f16 exactly.
+__device__ __forceinline__ uint32_t e4m3_round_f16x2(uint32_t h) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f16x2 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(h));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

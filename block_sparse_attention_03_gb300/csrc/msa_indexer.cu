@@ -91,7 +91,7 @@ __host__ __device__ constexpr int m_group() {
 template <int FMT, int NT, int SP>
 __device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* scales,
                                             const uint32_t (&bq)[SP][NT][IdxTraits<FMT>::KS][2], int lane, int key0,
-                                            const int (&lim)[NT][2], float (&cmax)[NT][2]) {
+                                            const int (&lim)[NT][2], float (&cmax)[NT][2], bool nvr = false) {
   constexpr int KS = IdxTraits<FMT>::KS;
   constexpr int MG = m_group<NT>();
   const int g = lane >> 2, j = lane & 3;
@@ -167,6 +167,10 @@ __device__ __forceinline__ void score_block(const uint8_t* tile, const uint8_t* 
           a[2] = *reinterpret_cast<uint32_t*>(&t);
           t = __hmul2(*reinterpret_cast<__half2*>(&x3), *reinterpret_cast<const __half2*>(&s1[mi][grp]));
           a[3] = *reinterpret_cast<uint32_t*>(&t);
+          if (nvr) {  // the product rounded to E4M3, as the Blackwell NVFP4 -> FP8 dequant does
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[q] = e4m3_round_f16x2(a[q]);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_f16_k16(acc[mi][nt], a, bq[0][nt][ks][0], bq[0][nt][ks][1]);
         }
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) cmax[nt][0] = cmax[nt][1] = -INFINITY;
         score_block<FMT, NT, SP>(tiles + (size_t)st * TR::TILE, scal + (size_t)st * LY::SC, bq, lane, b * kBlock,
-                                 lim, cmax);
+                                 lim, cmax, p.nv_round != 0);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

@@ -61,6 +61,7 @@ struct IndexerParams {
   int32_t iq_fp8;
   float iq_scale;          // per-tensor scale of e4m3 index queries
   float col_const;         // index_scale (x NVFP4 per-tensor scale)
+  int32_t nv_round;        // NVFP4 keys: e2m1 x e4m3 rounded to E4M3 (MSA_NVFP4_E4M3_PRODUCT)
   FragGeom geom;
   float* pooled;           // [S*Q][G][max_nb]
   DeviceStatus* status;
@@ -117,6 +118,7 @@ struct AttendParams {
   const float* k_scale;
   const float* v_scale;
   float v_global;           // NVFP4 V per-tensor scale (K's is folded into col_const)
+  int32_t nv_round;         // NVFP4 K / V: e2m1 x e4m3 rounded to E4M3 (MSA_NVFP4_E4M3_PRODUCT)
   const void* q;            // [S*Q][G*r][128] bf16 or e4m3 codes
   int32_t q_fp8;
   float q_scale;

@@ -86,6 +86,18 @@ typedef enum {
   MSA_DTYPE_NVFP4 = 2
 } msa_dtype_t;
 
+/* How an NVFP4 element's two factors combine (vLLM Day-0 blog, "NVIDIA
+ * Blackwell 优化的 MSA 内核": the Blackwell kernels dequantize NVFP4 to FP8 with
+ * mul.e4m3x4.e2m1x4.e4m3x4, i.e. the product is rounded to E4M3).
+ *   MSA_NVFP4_EXACT          e2m1 x e4m3 block scale exactly (it has at most six
+ *                            significant bits), then x the fp32 per-tensor scale;
+ *   MSA_NVFP4_E4M3_PRODUCT   the product rounded to E4M3 (nearest, ties to even,
+ *                            saturating at +-448) first, as that dequant does. */
+typedef enum {
+  MSA_NVFP4_EXACT = 0,
+  MSA_NVFP4_E4M3_PRODUCT = 1
+} msa_nvfp4_mode_t;
+
 /* The paged K/V cache and the index-key side cache of one attention layer.
  * K/V dtype and index dtype are independent (the model's
  * --kv-cache-dtype and indexer_kv_dtype settings).  Unused pointers (scales of
@@ -110,6 +122,7 @@ typedef struct {
   float k_global;       /* NVFP4 only */
   float v_global;
   float idx_global;
+  int32_t nvfp4_mode;   /* msa_nvfp4_mode_t, for every NVFP4 tensor of the cache (0 = exact) */
 } msa_cache_t;
 
 /* The batch: num_seqs sequences with q_per_seq new query tokens each.

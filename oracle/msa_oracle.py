@@ -105,7 +105,7 @@ def nvfp4_product_exact(nibble: int, scale_code: int) -> Fraction:
 # cache decode to fp32 (the values the whole path works on)
 # ----------------------------------------------------------------------------
 
-def _dequant(dtype, data, scale=None, sf=None, gscale=None) -> np.ndarray:
+def _dequant(dtype, data, scale=None, sf=None, gscale=None, nvfp4_mode="exact") -> np.ndarray:
     if dtype == "bf16":
         return bf16_value(data)
     if dtype == "fp8":
@@ -115,6 +115,13 @@ def _dequant(dtype, data, scale=None, sf=None, gscale=None) -> np.ndarray:
         vals = e2m1_value(unpack_e2m1(data))  # [..., D]
         sfv = e4m3_value(sf)  # [..., D/16]
         prod = (vals * np.repeat(sfv, 16, axis=-1)).astype(np.float32)  # exact
+        if nvfp4_mode == "e4m3":
+            # the product rounded to E4M3 first (nearest even, saturating), as
+            # the Blackwell kernels' NVFP4 -> FP8 dequant does (Day-0 blog,
+            # "NVIDIA Blackwell 优化的 MSA 内核")
+            prod = e4m3_value(e4m3_code(prod)).astype(np.float32)
+        elif nvfp4_mode != "exact":
+            raise ValueError(nvfp4_mode)
         return (prod * np.float32(gscale)).astype(np.float32)
     raise ValueError(dtype)
 
@@ -126,7 +133,7 @@ def dequant_kv_tile(case: dict, which: str, phys: int) -> np.ndarray:
     return _dequant(dt, case[which][phys],
                     case[which + "_scale"][phys] if dt == "fp8" else None,
                     case[which + "_sf"][phys] if dt == "nvfp4" else None,
-                    case.get(which + "_global"))
+                    case.get(which + "_global"), case.get("nvfp4_mode", "exact"))
 
 
 def dequant_index_tile(case: dict, phys: int) -> np.ndarray:
@@ -135,7 +142,7 @@ def dequant_index_tile(case: dict, phys: int) -> np.ndarray:
     return _dequant(dt, case["idx"][phys],
                     case["idx_scale"][phys] if dt == "fp8" else None,
                     case["idx_sf"][phys] if dt == "nvfp4" else None,
-                    case.get("idx_global"))
+                    case.get("idx_global"), case.get("nvfp4_mode", "exact"))
 
 
 def query_values(data, dtype: str, scale: float) -> np.ndarray:

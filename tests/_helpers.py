@@ -35,7 +35,7 @@ def bind(case: dict):
         k_sf=case.get("k_sf"), v_sf=case.get("v_sf"), k_scale=case.get("k_scale"),
         v_scale=case.get("v_scale"), idx_sf=case.get("idx_sf"), idx_scale=case.get("idx_scale"),
         k_global=case.get("k_global", 0.0), v_global=case.get("v_global", 0.0),
-        idx_global=case.get("idx_global", 0.0))
+        idx_global=case.get("idx_global", 0.0), nvfp4_mode=case.get("nvfp4_mode", "exact"))
     batch = msa.Batch(case["seq_lens"], case["block_table"], w.q_per_seq)
     iq = msa.Query(case["index_q"], w.q_dtype, case["index_q_scale"])
     q = msa.Query(case["q"], w.q_dtype, case["q_scale"])

@@ -63,10 +63,14 @@ def test_workspace_size_host_only(lib):
     assert n > 0
     assert lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 15) == 0
     for over in ({"f__topk": 12}, {"f__score_type": 1}, {"f__score_type": -1}, {"c__block_size": 64}, {"c__head_dim": 64}, {"b__num_seqs": 0},
-                 {"f__init_blocks": 16}, {"b__q_per_seq": 50 * 128 + 1}, {"c__num_kv_heads": 9}):
+                 {"f__init_blocks": 16}, {"b__q_per_seq": 50 * 128 + 1}, {"c__num_kv_heads": 9},
+                 {"c__nvfp4_mode": 2}, {"c__nvfp4_mode": -1}):
         c2, b2, f2 = _structs(**over)
         assert lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) == 0, over
     # more sequences or blocks never shrink the workspace
+    # both NVFP4 modes are valid descriptions
+    c4, b4, f4 = _structs(c__nvfp4_mode=1)
+    assert lib.msa_workspace_size(ctypes.byref(c4), ctypes.byref(b4), ctypes.byref(f4), 16) == n
     c3, b3, f3 = _structs(b__num_seqs=8, b__max_blocks_per_seq=500)
     assert lib.msa_workspace_size(ctypes.byref(c3), ctypes.byref(b3), ctypes.byref(f3), 16) > n
 

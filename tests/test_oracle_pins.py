@@ -547,3 +547,47 @@ def test_insert_writes_only_the_mapped_slots():
                                  gscale=c[name + "_global"])
             tol = 0 if kv == "bf16" else (0.07 if kv == "fp8" else 0.3)
             assert np.abs(got - ref).max() <= tol * np.abs(ref).max() + 1e-12, (kv, name)
+
+
+# ---------------------------------------------------------------- NVFP4 E4M3-product mode
+# The Blackwell kernels dequantize NVFP4 with the product e2m1 x e4m3 rounded to
+# E4M3 (Day-0 blog, "NVIDIA Blackwell 优化的 MSA 内核"); the oracle's "e4m3" mode
+# must equal torch's float8 cast of that exact product (clamped to +-448, the
+# saturating conversion), times the fp32 per-tensor scale afterwards.
+
+_E2M1_OCP = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def _all_products_tile():
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]  # every non-NaN scale code
+    nib = np.arange(16, dtype=np.uint8)
+    packed = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)  # element 2j in the low nibble
+    data = np.tile(packed, (len(codes), 1))                   # [codes][8]
+    sf = np.array(codes, dtype=np.uint8)[:, None]              # one scale per 16 elements
+    return codes, data, sf
+
+
+@pytest.mark.parametrize("g", [1.0, 0.75, 3.0e-3])
+def test_nvfp4_e4m3_product_mode_equals_torch_cast(g):
+    codes, data, sf = _all_products_tile()
+    got = O._dequant("nvfp4", data, sf=sf, gscale=g, nvfp4_mode="e4m3")
+    sc = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    prod = sc[:, None] * torch.tensor(_E2M1_OCP, dtype=torch.float64)[None, :]   # exact
+    rounded = prod.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).double()
+    ref = (rounded.float() * torch.tensor(g, dtype=torch.float32)).numpy()
+    assert np.array_equal(got.view(np.uint32), ref.astype(np.float32).view(np.uint32))
+
+
+def test_nvfp4_modes_differ_only_where_the_product_is_not_an_e4m3_value():
+    codes, data, sf = _all_products_tile()
+    exact = O._dequant("nvfp4", data, sf=sf, gscale=1.0)
+    rnd = O._dequant("nvfp4", data, sf=sf, gscale=1.0, nvfp4_mode="e4m3")
+    sc = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    prod = (sc[:, None] * torch.tensor(_E2M1_OCP, dtype=torch.float64)[None, :]).numpy()
+    representable = prod.clip(-448, 448) == torch.tensor(prod.clip(-448, 448)).to(torch.float8_e4m3fn).double().numpy()
+    representable &= np.abs(prod) <= 448
+    assert np.array_equal(exact[representable], rnd[representable])
+    assert (exact[~representable] != rnd[~representable]).all()
+    assert (~representable).sum() > 100  # the mode changes many products (e.g. 1.5 x 1.125)
+    with pytest.raises(ValueError):
+        O._dequant("nvfp4", data, sf=sf, gscale=1.0, nvfp4_mode="e5m2")
