@@ -89,15 +89,6 @@ static_assert(TqLayout::STAGE >= 32768 + 128 * 16, "an item's output rows fit it
 constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);
 
-// Operand descriptor of an MN-major 128-byte-swizzled tile: 128-byte rows
-// along K (one per key), 8-row groups 1024 bytes apart.  With 128 e4m3
-// columns the tile is one swizzle atom wide, so only the K-direction group
-// offset is used; both offsets hold it.
-__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)(1024 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 // D (TMEM) = / += A (TMEM, K-major rows = lanes) x B (smem)^T, e4m3, fp32 accumulate.
 __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -114,7 +105,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16-byte global -> shared copy (zero fill when !ok), completed by cp_async_wait.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {

@@ -72,6 +72,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory operand descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (the layout a 128-byte-swizzled TMA box of 128-byte rows
@@ -79,6 +80,15 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // for this layout (1); descriptor version 1; swizzle code 2 = 128 B.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Operand descriptor of an MN-major 128-byte-swizzled tile: 128-byte rows
+// along K (one per key), 8-row groups 1024 bytes apart.  With 128 e4m3
+// columns the tile is one swizzle atom wide, so only the K-direction group
+// offset is used; both offsets hold it.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)(1024 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
