@@ -218,6 +218,7 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
     const size_t L = (size_t)b->num_seqs * G * b->max_blocks_per_seq;
     const size_t E = (size_t)b->num_seqs * b->q_per_seq * G * cfg->topk;
     const size_t P = E * pl.r;
+    if (P >= ((size_t)1 << 31)) return MSA_ERR_UNSUPPORTED;  // the list kernels count entries and partials in 32 bits
     pl.off_kcnt = o; o = align256(o + L * 4);
     pl.off_koff = o; o = align256(o + L * 4);
     pl.off_kcur = o; o = align256(o + L * 4);

@@ -25,17 +25,19 @@ namespace {
 // earlier slot of the same row already names (the last two flagged once, by
 // the count pass; the softmax runs over the selected key set, each key once).
 // Count, fill and combine agree.
-__device__ __forceinline__ long k2q_list(const K2qParams& p, long e, bool flag) {
+// (Entries, rows and tokens are counted in 32 bits: make_plan keeps every
+// partial index below 2^31.)
+__device__ __forceinline__ long k2q_list(const K2qParams& p, int e, bool flag) {
   const BatchDev bt = p.batch;
   const int b = p.topk_idx[e];
   if (b < 0) return -1;
-  const long row = e / p.topk;  // token * G + g
-  const long token = row / p.G;
-  const int s = (int)(token / bt.Q), g = (int)(row % p.G), i = (int)(token % bt.Q);
+  const int row = e / p.topk;  // token * G + g
+  const int token = row / p.G;
+  const int s = token / bt.Q, g = row % p.G, i = token % bt.Q;
   const int T = bt.seq_len(s);
   bool bad = b >= bt.max_nb || T < bt.Q || T > bt.max_nb * kBlock || b > (T - bt.Q + i) / kBlock;
-  const int slot = (int)(e - row * p.topk);
-  for (int k = 0; k < slot && !bad; ++k) bad = p.topk_idx[row * p.topk + k] == b;
+  const int slot = e - row * p.topk;
+  for (int k = 0; k < slot && !bad; ++k) bad = p.topk_idx[(long)row * p.topk + k] == b;
   if (bad) {
     if (flag) raise_flag(p.status, FLAG_BAD_SELECT, b);
     return -1;
@@ -45,8 +47,8 @@ __device__ __forceinline__ long k2q_list(const K2qParams& p, long e, bool flag) 
 
 __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
-  const long n = (long)bt.S * bt.Q * p.G * p.topk;
-  for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
+  const int n = bt.S * bt.Q * p.G * p.topk;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
     const long key = k2q_list(p, e, true);
     if (key >= 0) atomicAdd(&p.cnt[key], 1);
   }
@@ -55,11 +57,11 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
   // q x 2^e with the largest e that keeps the row's amax at most 448 (exact),
   // split into e4m3 hi + lo (together all 8 significant bits of bf16), and
   // the row factor 2^-e x col_const
-  const long rows = (long)bt.S * bt.Q * p.G * p.r;
+  const int rows = bt.S * bt.Q * p.G * p.r;
   const int lane = threadIdx.x & 31;
-  const long nw = (long)gridDim.x * (blockDim.x >> 5);
-  for (long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q) + row * 128) + lane);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q) + (long)row * 128) + lane);
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
     float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
     split_e4m3(a.y * ps, h[1], l[1]);
     split_e4m3(b.x * ps, h[2], l[2]);
     split_e4m3(b.y * ps, h[3], l[3]);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(p.qsplit + row * 256);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.qsplit + (long)row * 256);
     dst[lane] = (uint32_t)pack_e4m3x2(h[0], h[1]) | ((uint32_t)pack_e4m3x2(h[2], h[3]) << 16);
     dst[32 + lane] = (uint32_t)pack_e4m3x2(l[0], l[1]) | ((uint32_t)pack_e4m3x2(l[2], l[3]) << 16);
     if (lane == 0) p.qrowf[row] = ldexpf(1.f, -ex) * p.col_const;
@@ -118,11 +120,11 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
 
 __global__ void __launch_bounds__(256) k2q_fill_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
-  const long n = (long)bt.S * bt.Q * p.G * p.topk;
-  for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long)gridDim.x * blockDim.x) {
+  const int n = bt.S * bt.Q * p.G * p.topk;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
     const long key = k2q_list(p, e, false);
     if (key < 0) continue;
-    const long token = e / p.topk / p.G;
+    const int token = e / p.topk / p.G;
     const int slot = (int)(e % p.topk);
     const int at = atomicAdd(&p.cur[key], 1);
     p.entries[at] = (int)(token * 32 + slot);
@@ -144,19 +146,19 @@ template <int KMAX>
 __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
   const int H = p.G * p.r;
-  const long rows = (long)bt.S * bt.Q * H;
+  const int rows = bt.S * bt.Q * H;
   const int lane = threadIdx.x & 31, half = lane >> 4, d8 = 8 * (lane & 15);
-  const long nw = (long)gridDim.x * (blockDim.x >> 5);
-  for (long row = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
-    const long token = row / H;
-    const int h = (int)(row % H), g = h / p.r;
-    const int32_t* sel = p.topk_idx + (token * p.G + g) * p.topk;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+    const int token = row / H;
+    const int h = row % H, g = h / p.r;
+    const int32_t* sel = p.topk_idx + ((long)token * p.G + g) * p.topk;
     // the entries the lists hold (k2q_list's rule), no others: the token's
     // visible blocks of a well-formed sequence
-    const int s = (int)(token / bt.Q), i = (int)(token % bt.Q);
+    const int s = token / bt.Q, i = token % bt.Q;
     const int T = bt.seq_len(s);
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
-    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + (token * p.topk * H + h) * 128 + d8);
+    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + ((long)token * p.topk * H + h) * 128 + d8);
     uint4 ov[KMAX / 2];
 #pragma unroll
     for (int q = 0; q < KMAX / 2; ++q) {  // slot 2q + half
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     if (lane < p.topk) {
       const int b = bl;
       if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
-        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + (token * p.topk + lane) * H + h);
+        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + ((long)token * p.topk + lane) * H + h);
         mk = ml.x;  // m, l, 2^ev
         lk = ml.y;
         fk = ml.z;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
       pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
       pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
       pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * 128 + d8) = pk;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (long)row * 128 + d8) = pk;
     }
     if (lane == 0 && p.lse) p.lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
   }

@@ -509,10 +509,10 @@ __global__ void __launch_bounds__(32 * kTopkWarpRows) topk_warp_kernel(const Top
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BatchDev bt = p.batch;
-  const long rows = (long)bt.S * bt.Q * p.G;
-  const long row = (long)blockIdx.x * kTopkWarpRows + warp;
+  const int rows = bt.S * bt.Q * p.G;  // below 2^31 (make_plan)
+  const int row = blockIdx.x * kTopkWarpRows + warp;
   if (row >= rows) return;
-  const int sq = (int)(row / p.G);
+  const int sq = row / p.G;
   const int s = sq / bt.Q, i = sq % bt.Q;
   const int T = bt.seq_len(s);
   int id = -1;
