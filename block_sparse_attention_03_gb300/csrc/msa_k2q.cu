@@ -165,18 +165,19 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
       const int k = 2 * q + half;
       ov[q] = k < p.topk ? __ldcg(orow + (long)k * H * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
+    // slot lane's (m, l, 2^ev), loaded with the rest (in bounds for every slot;
+    // used only for the slots the lists hold)
+    const float4 ml = lane < p.topk
+                          ? __ldcg(reinterpret_cast<const float4*>(p.part_ml) + ((long)token * p.topk + lane) * H + h)
+                          : make_float4(-INFINITY, 0.f, 1.f, 0.f);
     float mk = -INFINITY, lk = 0.f, fk = 1.f;
     const int bl = lane < p.topk ? sel[lane] : -1;
     // a block an earlier slot already names has no list entry (k2q_list)
     const unsigned same = __match_any_sync(0xffffffffu, bl);
-    if (lane < p.topk) {
-      const int b = bl;
-      if (b >= 0 && b <= last && (same & ((1u << lane) - 1u)) == 0u) {
-        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part_ml) + ((long)token * p.topk + lane) * H + h);
-        mk = ml.x;  // m, l, 2^ev
-        lk = ml.y;
-        fk = ml.z;
-      }
+    if (lane < p.topk && bl >= 0 && bl <= last && (same & ((1u << lane) - 1u)) == 0u) {
+      mk = ml.x;
+      lk = ml.y;
+      fk = ml.z;
     }
     float M = mk;
 #pragma unroll
