@@ -58,12 +58,15 @@ class MsaBatchT(ctypes.Structure):
 class MsaConfigT(ctypes.Structure):
     _fields_ = [("topk", ctypes.c_int32), ("init_blocks", ctypes.c_int32),
                 ("local_blocks", ctypes.c_int32), ("index_scale", ctypes.c_float),
-                ("sm_scale", ctypes.c_float), ("score_type", ctypes.c_int32)]
+                ("sm_scale", ctypes.c_float), ("score_type", ctypes.c_int32), ("prefill_select", ctypes.c_int32)]
 
 
-SCORE_TYPES = {"max": 0}
+SCORE_TYPES = {"max": 0}  # msa_score_type_t: the block pooling of the index scores
 # msa_nvfp4_mode_t: "exact" e2m1 x e4m3 products, or "e4m3": rounded to E4M3 first
-NVFP4_MODES = {"exact": 0, "e4m3": 1}  # msa_score_type_t: the block pooling of the index scores
+NVFP4_MODES = {"exact": 0, "e4m3": 1}
+# msa_prefill_select_t: a prefill chunk's selection by a top-k launch over the
+# pooled scores, or in the tcgen05 indexer's epilogue (candidate lists)
+PREFILL_SELECT = {"topk": 0, "indexer": 1}
 
 
 class MsaQueryT(ctypes.Structure):
@@ -171,11 +174,12 @@ class Config:
     index_scale: float = 128 ** -0.5
     sm_scale: float = 128 ** -0.5
     score_type: str = "max"
+    prefill_select: str = "topk"
 
     def struct(self) -> MsaConfigT:
         # an unknown score type reaches the library as -1, which rejects it
         return MsaConfigT(self.topk, self.init_blocks, self.local_blocks, self.index_scale, self.sm_scale,
-                          SCORE_TYPES.get(self.score_type, -1))
+                          SCORE_TYPES.get(self.score_type, -1), PREFILL_SELECT.get(self.prefill_select, -1))
 
 
 @dataclasses.dataclass

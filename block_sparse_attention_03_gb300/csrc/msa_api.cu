@@ -94,6 +94,8 @@ msa_status_t check_cfg(const msa_config_t* c) {
   if (!(c->index_scale > 0.f) || !std::isfinite(c->index_scale)) return MSA_ERR_INVALID_ARGUMENT;
   if (!(c->sm_scale > 0.f) || !std::isfinite(c->sm_scale)) return MSA_ERR_INVALID_ARGUMENT;
   if (c->score_type != MSA_SCORE_MAX) return MSA_ERR_UNSUPPORTED;
+  if (c->prefill_select != MSA_PREFILL_SELECT_TOPK && c->prefill_select != MSA_PREFILL_SELECT_INDEXER)
+    return MSA_ERR_INVALID_ARGUMENT;
   return MSA_OK;
 }
 
@@ -153,6 +155,10 @@ struct Plan {
   // prefill chunks over an FP8 cache: the key-block-major attend (selection lists,
   // one partial per (token, head, slot), a combine pass)
   bool k2q = false;
+  // ... whose selection the tcgen05 indexer makes in its epilogue (candidate
+  // lists and a merge launch instead of the pooled scores and a top-k launch)
+  bool pisel = false;
+  size_t off_plists = 0;
   size_t off_kcnt = 0, off_koff = 0, off_kcur = 0, off_kitem = 0, off_kent = 0, off_klist = 0, off_kpo = 0,
          off_kpml = 0, off_kq = 0, off_kqf = 0;
 };
@@ -168,7 +174,7 @@ bool tc_indexer(const msa_cache_t* c, const msa_batch_t* b) {
 
 // Plan for the given problem.  iq_fp8 / q_fp8: query dtypes (E4M3 or bf16).
 msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, int hq, bool iq_fp8,
-                       bool q_fp8, Plan& pl) {
+                       bool q_fp8, Plan& pl, bool allow_pisel = true) {
   // more than 8 new tokens per sequence (a prefill chunk): split into virtual
   // sequences of the largest of 8, 4, 2, 1 tokens dividing the count
   int QV = b->q_per_seq;
@@ -204,7 +210,12 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.nctr = S * G;  // splits finished per (sequence, group)
   size_t o = 0;
   pl.off_status = o; o = align256(o + 256);
-  pl.off_pooled = o; o = align256(o + (size_t)b->num_seqs * b->q_per_seq * G * b->max_blocks_per_seq * 4);
+  pl.k2q = fa == FMT_FP8 && b->q_per_seq > 8 && (pl.r == 1 || pl.r == 2 || pl.r == 4 || pl.r == 8);
+  // (16 list entries a thread, 16-bit block ids)
+  pl.pisel = allow_pisel && cfg->prefill_select == MSA_PREFILL_SELECT_INDEXER && pl.k2q && tc_indexer(c, b) &&
+             cfg->topk <= 16 && b->max_blocks_per_seq <= 65536;
+  pl.off_pooled = o;
+  if (!pl.pisel) o = align256(o + (size_t)b->num_seqs * b->q_per_seq * G * b->max_blocks_per_seq * 4);
   pl.off_uids = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_umask = o; o = align256(o + (size_t)S * G * pl.cap * 4);
   pl.off_ucount = o; o = align256(o + (size_t)S * G * 4);
@@ -213,7 +224,14 @@ msa_status_t make_plan(const msa_cache_t* c, const msa_batch_t* b, const msa_con
   pl.off_cfa = o; o = align256(o + (size_t)S * G * pl.ga.nt * 8 * 4);
   pl.off_po = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 128 * 4);
   pl.off_pml = o; o = align256(o + (size_t)S * G * pl.splits * pl.ga.cols * 2 * 4);
-  pl.k2q = fa == FMT_FP8 && b->q_per_seq > 8 && (pl.r == 1 || pl.r == 2 || pl.r == 4 || pl.r == 8);
+  if (pl.pisel) {
+    // a list slot per (CTA, query tile it touches): at most tiles + min(CTAs,
+    // units) slots of 128 rows x 4 lists x 16 keys
+    const size_t tiles = (size_t)b->num_seqs * ((b->q_per_seq + 128 / G - 1) / (128 / G));
+    const size_t units = tiles * (size_t)((b->max_blocks_per_seq + 1) / 2);
+    const size_t ctas = (size_t)prefill_indexer_grid(sm_count());
+    pl.off_plists = o; o = align256(o + (tiles + (units < ctas ? units : ctas)) * 128 * 64 * 8);
+  }
   if (pl.k2q) {
     const size_t L = (size_t)b->num_seqs * G * b->max_blocks_per_seq;
     const size_t E = (size_t)b->num_seqs * b->q_per_seq * G * cfg->topk;
@@ -266,7 +284,7 @@ msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA
 // ---------------------------------------------------------------- stages of the path
 
 msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* iq,
-                         const Plan& pl, void* ws, float* pooled, cudaStream_t st) {
+                         const Plan& pl, void* ws, float* pooled, cudaStream_t st, bool select = false) {
   const int G = c->num_kv_heads;
   const int fi = fmt_of(c->index_dtype);
   CUtensorMap tm;
@@ -291,6 +309,10 @@ msa_status_t run_indexer(const msa_cache_t* c, const msa_batch_t* b, const msa_c
     pp.iq_scale = pp.iq_fp8 ? iq->scale : 1.f;
     pp.col_const = cfg->index_scale;
     pp.pooled = pooled;
+    pp.lists = select ? at<uint64_t>(ws, pl.off_plists) : nullptr;
+    pp.topk = cfg->topk;
+    pp.init_blocks = cfg->init_blocks;
+    pp.local_blocks = cfg->local_blocks;
     pp.status = at<DeviceStatus>(ws, pl.off_status);
     return cuda_status(launch_prefill_indexer(tmp, pp, sm_count(), st));
   }
@@ -364,6 +386,26 @@ msa_status_t run_topk(const msa_batch_t* b, const msa_config_t* cfg, int G, cons
   // fragments or counters)
   if (warp_rows && !topk_score && !tp.frag && !tp.zero) return cuda_status(launch_topk_warp(tp, st, pdl));
   return cuda_status(launch_topk(tp, st, pdl));
+}
+
+// The prefill selection from the candidate lists the tcgen05 indexer left (Plan::pisel).
+msa_status_t run_pisel(const msa_batch_t* b, const msa_config_t* cfg, int G, int32_t* topk_idx, const Plan& pl,
+                       void* ws, cudaStream_t st) {
+  Plan real;
+  real.S = b->num_seqs;
+  real.Q = b->q_per_seq;
+  real.chunks = 1;
+  PiSelectParams sp;
+  sp.batch = batch_dev(b, real);
+  sp.G = G;
+  sp.topk = cfg->topk;
+  sp.init_blocks = cfg->init_blocks;
+  sp.local_blocks = cfg->local_blocks;
+  sp.grid = prefill_indexer_grid(sm_count());
+  sp.lists = at<uint64_t>(ws, pl.off_plists);
+  sp.topk_idx = topk_idx;
+  sp.status = at<DeviceStatus>(ws, pl.off_status);
+  return cuda_status(launch_prefill_select(sp, st));
 }
 
 msa_status_t run_attend(const msa_cache_t* c, const msa_batch_t* b, const msa_config_t* cfg, const msa_query_t* q,
@@ -579,10 +621,11 @@ msa_status_t msa_decode(const msa_cache_t* cache, const msa_batch_t* batch, cons
   if (workspace_bytes < pl.total) return MSA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = (cudaStream_t)stream;
   float* pooled = at<float>(workspace, pl.off_pooled);
-  if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st)) != MSA_OK) return s;
+  if ((s = run_indexer(cache, batch, cfg, index_q, pl, workspace, pooled, st, pl.pisel)) != MSA_OK) return s;
   if (pl.k2q) {
-    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true, false,
-                      nullptr, true)) != MSA_OK)
+    if ((s = pl.pisel ? run_pisel(batch, cfg, cache->num_kv_heads, topk_idx, pl, workspace, st)
+                      : run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, workspace, &pl, st, true,
+                                 false, nullptr, true)) != MSA_OK)
       return s;
     return run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, workspace, st);
   }
@@ -708,6 +751,10 @@ extern "C" msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_b
   if ((s = make_plan(cache, batch, cfg, num_q_heads, index_q->dtype == MSA_DTYPE_FP8_E4M3,
                      q->dtype == MSA_DTYPE_FP8_E4M3, pl)) != MSA_OK)
     return s;
+  if (pl.total > MSA_NOALLOC_SCRATCH_BYTES && pl.pisel &&
+      (s = make_plan(cache, batch, cfg, num_q_heads, index_q->dtype == MSA_DTYPE_FP8_E4M3,
+                     q->dtype == MSA_DTYPE_FP8_E4M3, pl, false)) != MSA_OK)  // pooled scores may still fit
+    return s;
   if (pl.total > MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   if ((s = noalloc_scratch(&ws)) != MSA_OK) return s;
@@ -715,11 +762,12 @@ extern "C" msa_status_t msa_decode_noalloc(const msa_cache_t* cache, const msa_b
   // the status word must start at zero; every other region is written before it is read
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MSA_ERR_CUDA;
   float* pooled = at<float>(ws, pl.off_pooled);
-  if ((s = run_indexer(cache, batch, cfg, index_q, pl, ws, pooled, st)) != MSA_OK) return s;
+  if ((s = run_indexer(cache, batch, cfg, index_q, pl, ws, pooled, st, pl.pisel)) != MSA_OK) return s;
   if (pl.k2q) {
     // a prefill chunk over an FP8 cache: the same chain as msa_decode's
-    if ((s = run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, false,
-                      nullptr, true)) != MSA_OK)
+    if ((s = pl.pisel ? run_pisel(batch, cfg, cache->num_kv_heads, topk_idx, pl, ws, st)
+                      : run_topk(batch, cfg, cache->num_kv_heads, pooled, topk_idx, nullptr, ws, &pl, st, true, false,
+                                 nullptr, true)) != MSA_OK)
       return s;
     if ((s = run_k2q(cache, batch, cfg, q, num_q_heads, topk_idx, out, lse, pl, ws, st)) != MSA_OK) return s;
   } else {

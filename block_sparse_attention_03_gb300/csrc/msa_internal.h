@@ -156,7 +156,27 @@ struct PrefillIndexerParams {
   int32_t iq_fp8;
   float iq_scale;
   float col_const;         // index_scale
-  float* pooled;
+  float* pooled;           // [S*Q][G][max_nb] (lists == null)
+  // Selection in the epilogue (lists != null, topk <= 16, max_nb <= 65536; no pooled scores):
+  // each epilogue thread keeps the 16 best free blocks (top-k rule order) of
+  // the blocks it scores for its row and writes them, per query tile it
+  // touched, as one list of 64-bit keys (order key of the score above, ~block
+  // id below; 0 = none) at slot (s * tiles + tile) + min(CTA index, the CTA's
+  // first unit): lists[slot][128 tile rows][4 epilogue groups][16].
+  uint64_t* lists;
+  int32_t topk, init_blocks, local_blocks;
+  DeviceStatus* status;
+};
+
+// The prefill selection from the indexer's candidate lists (one warp per
+// (token, group) row): the row's free blocks with the kfree largest keys, plus
+// the forced ones, ascending, as topk_kernel writes them.
+struct PiSelectParams {
+  BatchDev batch;            // the real batch
+  int32_t G, topk, init_blocks, local_blocks;
+  int32_t grid;              // CTAs of the indexer launch that wrote the lists
+  const uint64_t* lists;
+  int32_t* topk_idx;         // [S*Q][G][topk]
   DeviceStatus* status;
 };
 
@@ -211,6 +231,9 @@ cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, cons
 cudaError_t launch_k2q_combine(const K2qParams& p, cudaStream_t st);
 cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexerParams& p, int num_sms,
                                    cudaStream_t st);
+// the prefill indexer's grid (one CTA per SM)
+int prefill_indexer_grid(int num_sms);
+cudaError_t launch_prefill_select(const PiSelectParams& p, cudaStream_t st);
 cudaError_t launch_indexer(int fmt, const CUtensorMap* tmap, const IndexerParams& p, int num_sms, cudaStream_t st,
                            bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl);

@@ -145,6 +145,20 @@ typedef enum {
   MSA_SCORE_MAX = 0
 } msa_score_type_t;
 
+/* Where msa_decode selects the blocks of a prefill chunk over FP8 caches (more
+ * than 8 new tokens a sequence, the tcgen05 indexer).  The selection is the same
+ * either way, bit for bit; the two differ in time and workspace. */
+typedef enum {
+  /* the indexer writes every pooled score, a top-k launch reads them back
+     (default: the faster of the two on a 64K-token context) */
+  MSA_PREFILL_SELECT_TOPK = 0,
+  /* the indexer's epilogue keeps each row's 16 best free blocks as candidate
+     lists and a merge launch picks from them: no pooled scores, so the
+     workspace does not grow with the context length; topk <= 16 (otherwise,
+     and in msa_decode_noalloc when the lists do not fit, the top-k launch) */
+  MSA_PREFILL_SELECT_INDEXER = 1
+} msa_prefill_select_t;
+
 /* Method settings (the indexer's constructor arguments in the model). */
 typedef struct {
   int32_t topk;         /* blocks kept per (query, group): 4, 8, 16 or 32 */
@@ -153,6 +167,7 @@ typedef struct {
   float index_scale;    /* multiplies the index scores; model: index_dim ** -0.5 */
   float sm_scale;       /* softmax scale; model: head_dim ** -0.5 */
   int32_t score_type;   /* msa_score_type_t; 0 (max) in a zero-initialised struct */
+  int32_t prefill_select; /* msa_prefill_select_t; 0 (top-k launch) in a zero-initialised struct */
 } msa_config_t;
 
 /* A query tensor: BF16, or FP8 E4M3 codes times one fp32 per-tensor scale. */

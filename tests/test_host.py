@@ -64,7 +64,8 @@ def test_workspace_size_host_only(lib):
     assert lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 15) == 0
     for over in ({"f__topk": 12}, {"f__score_type": 1}, {"f__score_type": -1}, {"c__block_size": 64}, {"c__head_dim": 64}, {"b__num_seqs": 0},
                  {"f__init_blocks": 16}, {"b__q_per_seq": 50 * 128 + 1}, {"c__num_kv_heads": 9},
-                 {"c__nvfp4_mode": 2}, {"c__nvfp4_mode": -1}):
+                 {"c__nvfp4_mode": 2}, {"c__nvfp4_mode": -1}, {"f__prefill_select": 2},
+                 {"f__prefill_select": -1}):
         c2, b2, f2 = _structs(**over)
         assert lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) == 0, over
     # more sequences or blocks never shrink the workspace
@@ -118,6 +119,28 @@ def test_prefill_workspace_holds_the_partials(lib):
     c2, b2, f2 = _structs(b__num_seqs=1, b__q_per_seq=8192, b__max_blocks_per_seq=576, c__num_blocks=600,
                           c__kv_dtype=2)
     assert 0 < lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16) < n
+
+
+def test_prefill_select_in_indexer_needs_no_pooled_scores(lib):
+    # a prefill chunk (2048 new tokens on 256K keys, FP8 caches): selecting in
+    # the indexer's epilogue replaces the pooled scores (2048 x 4 groups x 2048
+    # blocks x 4 B = 64 MiB) with candidate lists of a fixed size per query tile
+    import block_sparse_attention_03_gb300 as msa
+    big = dict(b__num_seqs=1, b__q_per_seq=2048, b__max_blocks_per_seq=2048, c__num_blocks=4096)
+    c, b, f = _structs(**big)
+    topk_ws = lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 16)
+    c, b, f = _structs(f__prefill_select=1, **big)
+    lists_ws = lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 16)
+    # 64 MiB of pooled scores against (64 tiles + at most 148-152 CTAs) x 64 KiB of lists
+    assert 0 < lists_ws <= topk_ws - (64 << 20) + 216 * (64 << 10)
+    # topk 32 keeps the top-k launch (the lists hold 16 blocks a thread)
+    c, b, f = _structs(f__prefill_select=1, f__topk=32, **big)
+    c2, b2, f2 = _structs(f__topk=32, **big)
+    assert lib.msa_workspace_size(ctypes.byref(c), ctypes.byref(b), ctypes.byref(f), 16) == \
+        lib.msa_workspace_size(ctypes.byref(c2), ctypes.byref(b2), ctypes.byref(f2), 16)
+    assert msa.Config(prefill_select="indexer").struct().prefill_select == 1
+    assert msa.Config().struct().prefill_select == 0
+    assert msa.Config(prefill_select="other").struct().prefill_select == -1
 
 
 def test_score_type_other_than_max_is_unsupported(lib):

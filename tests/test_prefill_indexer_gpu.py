@@ -119,17 +119,35 @@ def test_prefill_bad_block_flags_and_leaves_it_out():
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("zero_idx,init,local", [(False, 0, 0), (True, 0, 0), (False, 2, 3)])
-def test_prefill_warp_topk_equals_block_topk(zero_idx, init, local):
-    # msa_decode of a prefill chunk selects with one warp per row; the staged
-    # msa_topk_blocks (one CTA per row, checked against the oracle in
-    # test_topk_gpu.py) must give the same rows on the same pooled scores,
-    # ties included (a zero index cache ties every block)
-    w = ms.make_workload("fp8_prefill", seed=86, seq_lens=(128 * 40 + 5, 3000), q_per_seq=48)
+@pytest.mark.parametrize("mode,zero_idx,init,local,over", [
+    ("topk", False, 0, 0, None),
+    ("topk", True, 0, 0, None),
+    ("topk", False, 2, 3, None),
+    ("indexer", False, 0, 0, None),
+    ("indexer", True, 0, 0, None),
+    ("indexer", False, 2, 3, None),
+    # every query tile scored by several CTAs (about 17 units a CTA, 79 a tile)
+    ("indexer", False, 0, 0, dict(seq_lens=(20000,), q_per_seq=1024)),
+    # more CTAs a tile than the merge holds in registers
+    ("indexer", False, 0, 1, dict(seq_lens=(128 * 300,), q_per_seq=256)),
+    # a tile split between two CTAs, as in the full-size chunk (~200 units a CTA, 235 a tile)
+    ("indexer", False, 1, 2, dict(seq_lens=(60000,), q_per_seq=4096)),
+    ("indexer", True, 0, 0, dict(seq_lens=(60000,), q_per_seq=4096)),
+])
+def test_prefill_selection_equals_block_topk(mode, zero_idx, init, local, over):
+    # msa_decode of a prefill chunk selects either with one warp per row over
+    # the pooled scores ("topk") or in the tcgen05 indexer's epilogue
+    # ("indexer": per-thread running top-16 lists, merged a warp per row); the
+    # staged msa_indexer_score + msa_topk_blocks (a CTA per row on the pooled
+    # scores, checked against the oracle in test_topk_gpu.py) must give the same
+    # rows, ties included (a zero index cache ties every block).  The small case
+    # has more CTAs than units, so a tile's CTAs include some without units.
+    over = over or dict(seq_lens=(128 * 40 + 5, 3000), q_per_seq=48)
+    w = ms.make_workload("fp8_prefill", seed=86, **over)
     c = ms.make_case(w, device="cuda")
     if zero_idx:
         c["idx"].zero_()
-    cfg = msa.Config(topk=16, init_blocks=init, local_blocks=local)
+    cfg = msa.Config(topk=16, init_blocks=init, local_blocks=local, prefill_select=mode)
     cache, batch, iq, q = bind(c)
     ws = workspace(cache, batch, cfg, w.num_q_heads)
     rows, G = w.num_seqs * w.q_per_seq, w.num_kv_heads
