@@ -16,6 +16,7 @@ collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -413,6 +414,21 @@ def measure_workload(msa, B, st, steps, warmup, peak_gbs, peak_tf_e4m3):
                        "frac": fa / (att_ms * 1e-3) / 1e12 / peak_tf_e4m3},
         }
         res["path_tflops"] = (fi + fa) / (ms_step * 1e-3) / 1e12
+        # the same step with the selection made in the indexer's epilogue (no pooled scores)
+        cfg2 = dataclasses.replace(st["cfg"], prefill_select="indexer")
+        n2 = msa.msa_workspace_size(st["cache"], st["batch"], cfg2, w.num_q_heads)
+        ws2 = torch.empty(n2, dtype=torch.uint8, device=B.dev)
+        msa.msa_workspace_init(ws2)
+        topk3 = torch.empty_like(st["topk"])
+        ms_sel = B.time(lambda: msa.msa_decode(st["cache"], st["batch"], cfg2, st["iq"], st["q"], w.num_q_heads,
+                                               topk3, out2, None, ws2, stream), n_alone, warmup=3)
+        s_, flags = msa.msa_read_device_status(ws2)
+        if s_ != 0:
+            raise RuntimeError(f"{w.name} (indexer selection): device status {msa.msa_status_string(s_)} flags {flags}")
+        res["prefill_select_indexer"] = {
+            "ms_per_step": ms_sel, "workspace_mib": n2 / 2**20, "workspace_mib_topk": st["ws"].numel() / 2**20,
+            "same_selection": bool(torch.equal(topk3, st["topk"]))}
+        del ws2
     else:
         res["stage_roofline"] = {
             "indexer": {"bound": "hbm", "achieved": idx_bytes / (idx_ms * 1e-3) / 1e9, "unit": "GB/s",
