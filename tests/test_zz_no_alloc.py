@@ -6,6 +6,7 @@ match msa_decode's; two calls in a row check that the shared scratch carries
 nothing stale from one call into the next.  This file is collected last."""
 
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -25,10 +26,10 @@ def built():
     _build.build()
 
 
-def _with_workspace(case):
+def _with_workspace(case, **cfg_over):
     w = case["workload"]
     cache, batch, iq, q = bind(case)
-    cfg = msa.default_config(w.topk)
+    cfg = dataclasses.replace(msa.default_config(w.topk), **cfg_over)
     ws = workspace(cache, batch, cfg, w.num_q_heads)
     rows = w.num_seqs * w.q_per_seq
     topk = torch.empty((rows, w.num_kv_heads, w.topk), dtype=torch.int32, device="cuda")
@@ -39,10 +40,10 @@ def _with_workspace(case):
     return topk.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def _without_workspace(case):
+def _without_workspace(case, **cfg_over):
     w = case["workload"]
     cache, batch, iq, q = bind(case)
-    cfg = msa.default_config(w.topk)
+    cfg = dataclasses.replace(msa.default_config(w.topk), **cfg_over)
     rows = w.num_seqs * w.q_per_seq
     topk = torch.full((rows, w.num_kv_heads, w.topk), -5, dtype=torch.int32, device="cuda")
     out = torch.full((rows, w.num_q_heads, 128), 9.0, dtype=torch.bfloat16, device="cuda")
@@ -68,6 +69,26 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         err = np.abs(o - o_ref)
         assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS
         assert np.abs(l - l_ref).max() <= 1e-3
+
+
+@pytest.mark.parametrize("seq_len,lists_fit", [(1300, True), (40000, False)])
+def test_noalloc_prefill_with_selection_in_the_indexer(seq_len, lists_fit):
+    # prefill_select="indexer": where the candidate lists fit the scratch the
+    # chain uses them; where they do not (one query tile over 157 units, one list
+    # slot per CTA) but the pooled scores do, it falls back to the top-k launch.
+    # Either way the results equal msa_decode's with its default selection.
+    w = ms.make_workload("fp8_prefill", seq_lens=(seq_len,), q_per_seq=24, seed=95)
+    case = ms.make_case(w, device="cuda")
+    cache, batch, _, _ = bind(case)
+    sel = dataclasses.replace(msa.default_config(w.topk), prefill_select="indexer")
+    assert (msa.msa_workspace_size(cache, batch, sel, w.num_q_heads) <= 8 << 20) == lists_fit
+    assert msa.msa_workspace_size(cache, batch, msa.default_config(w.topk), w.num_q_heads) <= 8 << 20
+    t_ref, o_ref, l_ref = _with_workspace(case)
+    t, o, l = _without_workspace(case, prefill_select="indexer")
+    assert np.array_equal(t, t_ref)
+    err = np.abs(o - o_ref)
+    assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS
+    assert np.abs(l - l_ref).max() <= 1e-3
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
