@@ -363,6 +363,9 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
     const int4 inf = info_at(it);
     if (inf.x == -3) break;
     const long u = v0 + it;
+    // the kernels that follow may start their prologues once every warp is on
+    // its last unit (they still wait for this grid to finish before reading P)
+    if (u == v1 - 1) pdl_launch_dependents();
     const int st = (int)(it % NST);
     const int s = inf.z, b = inf.w;
     float* prow = p.pooled + (size_t)s * Q * G * bt.max_nb + b;
