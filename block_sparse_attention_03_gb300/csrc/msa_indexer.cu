@@ -326,18 +326,21 @@ __global__ void __launch_bounds__(IdxTraits<FMT>::WARPS * 32)
       const int phys = inf.x;
       uint8_t* dst = tiles + (size_t)st * TR::TILE;
       fence_proxy_async();
+      // the keys are read once: evict-first, so that they do not push the
+      // block tables, scores and code of the kernels that follow out of L2
+      const uint64_t pol = l2_policy_evict_first();
       if constexpr (FMT == FMT_FP8) {
         mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
-        tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
-        bulk_g2s(scal + (size_t)st * LY::SC, p.idx_scale + (size_t)phys * kBlock, TR::SCALES, &bars[st]);
+        tma_load_2d_hint(dst, &tmap, 0, phys * kBlock, &bars[st], pol);
+        bulk_g2s_hint(scal + (size_t)st * LY::SC, p.idx_scale + (size_t)phys * kBlock, TR::SCALES, &bars[st], pol);
       } else if constexpr (FMT == FMT_BF16) {
         mbar_expect_tx(&bars[st], TR::TILE);
-        tma_load_2d(dst, &tmap, 0, phys * kBlock, &bars[st]);
-        tma_load_2d(dst + 128 * 128, &tmap, 64, phys * kBlock, &bars[st]);
+        tma_load_2d_hint(dst, &tmap, 0, phys * kBlock, &bars[st], pol);
+        tma_load_2d_hint(dst + 128 * 128, &tmap, 64, phys * kBlock, &bars[st], pol);
       } else {
         mbar_expect_tx(&bars[st], TR::TILE + TR::SCALES);
-        bulk_g2s(dst, p.idx + (size_t)phys * TR::TILE, TR::TILE, &bars[st]);
-        bulk_g2s(scal + (size_t)st * LY::SC, p.idx_sf + (size_t)phys * TR::SCALES, TR::SCALES, &bars[st]);
+        bulk_g2s_hint(dst, p.idx + (size_t)phys * TR::TILE, TR::TILE, &bars[st], pol);
+        bulk_g2s_hint(scal + (size_t)st * LY::SC, p.idx_sf + (size_t)phys * TR::SCALES, TR::SCALES, &bars[st], pol);
       }
     }
   };
