@@ -223,11 +223,13 @@ def test_many_short_sequences():
         check_out(g["out"][[s]], o)
 
 
-def test_full_size_prefill_sampled():
-    # 8,192 new tokens on a 64K-token FP8 context: sampled query rows against the oracle
+@pytest.mark.parametrize("mode", ["topk", "indexer"])
+def test_full_size_prefill_sampled(mode):
+    # 8,192 new tokens on a 64K-token FP8 context: sampled query rows against the
+    # oracle, with the selection by the top-k launch or in the indexer's epilogue
     w = ms.make_workload("fp8_prefill")
     c = ms.make_case(w, device="cuda")
-    g = gpu_path(c)
+    g = gpu_path(c, cfg=msa.Config(topk=w.topk, prefill_select=mode))
     h = ms.case_to_host(c)
     del c
     torch.cuda.empty_cache()
