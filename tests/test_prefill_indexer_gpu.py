@@ -100,6 +100,31 @@ def test_prefill_indexer_bad_seq_len_flags_and_fills():
     check_pooled(got[:32], ref[:32])
 
 
+@pytest.mark.parametrize("mode", ["topk", "indexer"])
+def test_prefill_selection_of_a_bad_sequence(mode):
+    # a sequence shorter than its new tokens next to a good one: its rows are
+    # all -1 and the status says so, whichever way the chunk is selected; the
+    # good sequence's rows equal the staged top-k's
+    w = ms.make_workload("fp8_prefill", seed=88, seq_lens=(3000, 2000), q_per_seq=40)
+    c = ms.make_case(w, device="cuda")
+    c["seq_lens"][1] = 30
+    cfg = msa.Config(topk=16, prefill_select=mode)
+    cache, batch, iq, q = bind(c)
+    ws = workspace(cache, batch, cfg, w.num_q_heads)
+    rows, G = w.num_seqs * w.q_per_seq, w.num_kv_heads
+    topk = torch.full((rows, G, 16), -7, dtype=torch.int32, device="cuda")
+    out = torch.empty((rows, w.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, None, ws)
+    st, flags = msa.msa_read_device_status(ws)
+    assert st != 0 and flags & 2
+    assert (topk[40:] == -1).all()
+    pooled = torch.empty((rows, G, w.max_blocks), dtype=torch.float32, device="cuda")
+    msa.msa_indexer_score(cache, batch, cfg, iq, pooled, ws)
+    ref = torch.full_like(topk, -9)
+    msa.msa_topk_blocks(batch, cfg, G, pooled, ref, None, ws)
+    assert torch.equal(topk[:40], ref[:40])
+
+
 def test_prefill_bad_block_flags_and_leaves_it_out():
     # a block-table entry outside the pool in a prefill chunk: the status word
     # says so, and the attend leaves the block out (finite outputs, no stale partials)
@@ -119,22 +144,26 @@ def test_prefill_bad_block_flags_and_leaves_it_out():
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("mode,zero_idx,init,local,over", [
-    ("topk", False, 0, 0, None),
-    ("topk", True, 0, 0, None),
-    ("topk", False, 2, 3, None),
-    ("indexer", False, 0, 0, None),
-    ("indexer", True, 0, 0, None),
-    ("indexer", False, 2, 3, None),
+@pytest.mark.parametrize("mode,zero_idx,init,local,k,over", [
+    ("topk", False, 0, 0, 16, None),
+    ("topk", True, 0, 0, 16, None),
+    ("topk", False, 2, 3, 16, None),
+    ("topk", False, 8, 7, 16, None),        # the forced blocks fill every slot (kfree = 0)
+    ("indexer", False, 0, 0, 16, None),
+    ("indexer", True, 0, 0, 16, None),
+    ("indexer", False, 2, 3, 16, None),
+    ("indexer", False, 8, 7, 16, None),
+    ("indexer", False, 0, 0, 4, None),
+    ("indexer", True, 1, 1, 8, None),
     # every query tile scored by several CTAs (about 17 units a CTA, 79 a tile)
-    ("indexer", False, 0, 0, dict(seq_lens=(20000,), q_per_seq=1024)),
+    ("indexer", False, 0, 0, 16, dict(seq_lens=(20000,), q_per_seq=1024)),
     # more CTAs a tile than the merge holds in registers
-    ("indexer", False, 0, 1, dict(seq_lens=(128 * 300,), q_per_seq=256)),
+    ("indexer", False, 0, 1, 16, dict(seq_lens=(128 * 300,), q_per_seq=256)),
     # a tile split between two CTAs, as in the full-size chunk (~200 units a CTA, 235 a tile)
-    ("indexer", False, 1, 2, dict(seq_lens=(60000,), q_per_seq=4096)),
-    ("indexer", True, 0, 0, dict(seq_lens=(60000,), q_per_seq=4096)),
+    ("indexer", False, 1, 2, 16, dict(seq_lens=(60000,), q_per_seq=4096)),
+    ("indexer", True, 0, 0, 16, dict(seq_lens=(60000,), q_per_seq=4096)),
 ])
-def test_prefill_selection_equals_block_topk(mode, zero_idx, init, local, over):
+def test_prefill_selection_equals_block_topk(mode, zero_idx, init, local, k, over):
     # msa_decode of a prefill chunk selects either with one warp per row over
     # the pooled scores ("topk") or in the tcgen05 indexer's epilogue
     # ("indexer": per-thread running top-16 lists, merged a warp per row); the
@@ -147,11 +176,11 @@ def test_prefill_selection_equals_block_topk(mode, zero_idx, init, local, over):
     c = ms.make_case(w, device="cuda")
     if zero_idx:
         c["idx"].zero_()
-    cfg = msa.Config(topk=16, init_blocks=init, local_blocks=local, prefill_select=mode)
+    cfg = msa.Config(topk=k, init_blocks=init, local_blocks=local, prefill_select=mode)
     cache, batch, iq, q = bind(c)
     ws = workspace(cache, batch, cfg, w.num_q_heads)
     rows, G = w.num_seqs * w.q_per_seq, w.num_kv_heads
-    topk = torch.full((rows, G, 16), -7, dtype=torch.int32, device="cuda")
+    topk = torch.full((rows, G, k), -7, dtype=torch.int32, device="cuda")
     out = torch.empty((rows, w.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
     msa.msa_decode(cache, batch, cfg, iq, q, w.num_q_heads, topk, out, None, ws)
     pooled = torch.empty((rows, G, w.max_blocks), dtype=torch.float32, device="cuda")
