@@ -95,15 +95,16 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const TopkParams p) {
     write_qfrag(p.q, p.q_fp8, row_of, p.q_scale, p.col_const, p.key_fmt, p.geom, qs, pscale,
                 p.frag + (size_t)row * p.geom.words_per_unit(), p.colf + (size_t)row * p.geom.nt * 8);
   }
+  // the row's facts come from the caller's sequence lengths: read before the wait
+  const int sq = row / p.G;
+  const int s = sq / bt.Q, i = sq % bt.Q;
+  const int T = real_row ? bt.seq_len(s) : 0;
   pdl_wait();
   if (p.zero) {  // clear the attend's work counters for this call
     const int z = blockIdx.x * blockDim.x + threadIdx.x;
     if (z < p.nzero) p.zero[z] = 0;
   }
   if (!real_row) return;  // extra CTAs only clear counters
-  const int sq = row / p.G;
-  const int s = sq / bt.Q, i = sq % bt.Q;
-  const int T = bt.seq_len(s);
   const int K = p.topk;
   int32_t* out = p.topk_idx + (size_t)row * K;
   float* out_sc = p.topk_score ? p.topk_score + (size_t)row * K : nullptr;
@@ -526,15 +527,16 @@ __global__ void __launch_bounds__(32 * kTopkWarpRows) topk_warp_kernel(const Top
   __shared__ int hist[kTopkWarpRows][256];
   __shared__ int outb[kTopkWarpRows][32];
   pdl_launch_dependents();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BatchDev bt = p.batch;
   const int rows = bt.S * bt.Q * p.G;  // below 2^31 (make_plan)
   const int row = blockIdx.x * kTopkWarpRows + warp;
-  if (row >= rows) return;
+  // the row's facts come from the caller's sequence lengths: read before the wait
   const int sq = row / p.G;
   const int s = sq / bt.Q, i = sq % bt.Q;
-  const int T = bt.seq_len(s);
+  const int T = row < rows ? bt.seq_len(s) : 0;
+  pdl_wait();
+  if (row >= rows) return;
   int id = -1;
   if (T < bt.Q || T > bt.max_nb * kBlock) {
     if (lane == 0 && i == 0 && row % p.G == 0) raise_flag(p.status, FLAG_BAD_SEQLEN, s);
