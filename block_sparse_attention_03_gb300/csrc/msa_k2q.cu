@@ -4,8 +4,10 @@
 // per-block partials.
 //
 // Count: for every (token, group, slot) whose selected block is b, one more
-// entry in list (sequence, group, b); the same pass splits each bf16 query row
-// into the e4m3 hi + lo terms the attend's MMA reads.  Scan (one CTA): each
+// entry in list (sequence, group, b) -- taken token-fastest, so that a warp's
+// lanes mostly share lists and one atomic serves each group of them; the same
+// pass splits each bf16 query row into the e4m3 hi + lo terms the attend's MMA
+// reads.  Scan (one CTA): each
 // list's first entry and first attend item (item_tokens = 128 / r entries an
 // item: one MMA row per (token, head)).  Fill: every entry (token * 32 + slot)
 // into its list, in arrival order (the per-entry results do not depend on
@@ -45,12 +47,29 @@ __device__ __forceinline__ long k2q_list(const K2qParams& p, int e, bool flag) {
   return ((long)s * p.G + g) * bt.max_nb + b;
 }
 
+// Entry x of the count and fill passes, token-fastest: the lanes of a warp take
+// the same (group, slot) of 32 consecutive tokens, which often name the same
+// block (the slots are ascending; nearby tokens share their own and the best
+// blocks), so that one atomic serves each group of lanes with the same list.
+__device__ __forceinline__ int k2q_entry_of(const K2qParams& p, int x, int ntok) {
+  const int token = x % ntok, r = x / ntok;
+  const int g = r % p.G, slot = r / p.G;
+  return (token * p.G + g) * p.topk + slot;
+}
+
 __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
-  const int n = bt.S * bt.Q * p.G * p.topk;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-    const long key = k2q_list(p, e, true);
-    if (key >= 0) atomicAdd(&p.cnt[key], 1);
+  const int ntok = bt.S * bt.Q;
+  const int n = ntok * p.G * p.topk;
+  const int lane = threadIdx.x & 31;
+  for (int x0 = blockIdx.x * blockDim.x + (threadIdx.x & ~31); x0 < n; x0 += gridDim.x * blockDim.x) {
+    const int x = x0 + lane;  // the loop is warp-uniform
+    const long key = x < n ? k2q_list(p, k2q_entry_of(p, x, ntok), true) : -1;
+    const unsigned act = __ballot_sync(0xffffffffu, key >= 0);
+    if (key >= 0) {
+      const unsigned peers = __match_any_sync(act, (unsigned long long)key);
+      if (lane == __ffs(peers) - 1) atomicAdd(&p.cnt[key], __popc(peers));
+    }
   }
   if (p.q_fp8) return;
   // bf16 query rows (token, head), a warp each, lane l holding dims 4l .. 4l+3:
@@ -58,7 +77,6 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
   // split into e4m3 hi + lo (together all 8 significant bits of bf16), and
   // the row factor 2^-e x col_const
   const int rows = bt.S * bt.Q * p.G * p.r;
-  const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * (blockDim.x >> 5);
   for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q) + (long)row * 128) + lane);
@@ -120,14 +138,25 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
 
 __global__ void __launch_bounds__(256) k2q_fill_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
-  const int n = bt.S * bt.Q * p.G * p.topk;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
-    const long key = k2q_list(p, e, false);
-    if (key < 0) continue;
-    const int token = e / p.topk / p.G;
-    const int slot = (int)(e % p.topk);
-    const int at = atomicAdd(&p.cur[key], 1);
-    p.entries[at] = (int)(token * 32 + slot);
+  const int ntok = bt.S * bt.Q;
+  const int n = ntok * p.G * p.topk;
+  const int lane = threadIdx.x & 31;
+  for (int x0 = blockIdx.x * blockDim.x + (threadIdx.x & ~31); x0 < n; x0 += gridDim.x * blockDim.x) {
+    const int x = x0 + lane;  // the loop is warp-uniform
+    const int e = x < n ? k2q_entry_of(p, x, ntok) : 0;
+    const long key = x < n ? k2q_list(p, e, false) : -1;
+    const unsigned act = __ballot_sync(0xffffffffu, key >= 0);
+    if (key >= 0) {
+      // one cursor bump per group of lanes with the same list, each lane its place in it
+      const unsigned peers = __match_any_sync(act, (unsigned long long)key);
+      const int leader = __ffs(peers) - 1;
+      int at = 0;
+      if (lane == leader) at = atomicAdd(&p.cur[key], __popc(peers));
+      at = __shfl_sync(peers, at, leader) + __popc(peers & ((1u << lane) - 1u));
+      const int token = e / p.topk / p.G;
+      const int slot = e % p.topk;
+      p.entries[at] = token * 32 + slot;
+    }
   }
 }
 
