@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
 
 // One CTA of 1024 threads: thread t owns the contiguous lists [t*L/1024, (t+1)*L/1024).
 __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
-  __shared__ int se[1024], si[1024];
+  __shared__ int se[64], si[64];  // the warp totals, then their inclusive scan
   const BatchDev bt = p.batch;
   const long L = (long)bt.S * p.G * bt.max_nb;
   const int t = threadIdx.x;
@@ -112,17 +112,39 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
     ne += c;
     ni += (c + p.item_tokens - 1) / p.item_tokens;
   }
-  se[t] = ne;
-  si[t] = ni;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scans
-    const int ae = t >= o ? se[t - o] : 0, ai = t >= o ? si[t - o] : 0;
-    __syncthreads();
-    se[t] += ae;
-    si[t] += ai;
-    __syncthreads();
+  // inclusive scans of (entries, items) over the threads: within each warp by
+  // shuffles, then over the 32 warp totals by warp 0
+  const int lane = t & 31, warp = t >> 5;
+  int xe = ne, xi = ni;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ye = __shfl_up_sync(0xffffffffu, xe, o), yi = __shfl_up_sync(0xffffffffu, xi, o);
+    if (lane >= o) {
+      xe += ye;
+      xi += yi;
+    }
   }
-  int e0 = se[t] - ne, i0 = si[t] - ni;
+  if (lane == 31) {
+    se[warp] = xe;
+    si[warp] = xi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int ve = se[lane], vi = si[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ye = __shfl_up_sync(0xffffffffu, ve, o), yi = __shfl_up_sync(0xffffffffu, vi, o);
+      if (lane >= o) {
+        ve += ye;
+        vi += yi;
+      }
+    }
+    se[32 + lane] = ve;  // inclusive over warps
+    si[32 + lane] = vi;
+  }
+  __syncthreads();
+  const int be = warp > 0 ? se[32 + warp - 1] : 0, bi = warp > 0 ? si[32 + warp - 1] : 0;
+  int e0 = be + xe - ne, i0 = bi + xi - ni;
   for (long i = l0; i < l1; ++i) {
     const int c = p.cnt[i];
     const int items = (c + p.item_tokens - 1) / p.item_tokens;
@@ -133,7 +155,7 @@ __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
     e0 += c;
     i0 += items;
   }
-  if (t == 1023) p.item_off[L] = si[1023];
+  if (t == 1023) p.item_off[L] = si[32 + 31];
 }
 
 __global__ void __launch_bounds__(256) k2q_fill_kernel(const K2qParams p) {
