@@ -228,7 +228,7 @@ cudaError_t launch_insert(const InsertParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st);    // count, scan, fill
 cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms,
                               cudaStream_t st);
-cudaError_t launch_k2q_combine(const K2qParams& p, cudaStream_t st);
+cudaError_t launch_k2q_combine(const K2qParams& p, int num_sms, cudaStream_t st);
 cudaError_t launch_prefill_indexer(const CUtensorMap* tmap, const PrefillIndexerParams& p, int num_sms,
                                    cudaStream_t st);
 // the prefill indexer's grid (one CTA per SM)
