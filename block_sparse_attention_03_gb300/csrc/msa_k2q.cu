@@ -286,8 +286,8 @@ cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st) {
 cudaError_t launch_k2q_combine(const K2qParams& p, int num_sms, cudaStream_t st) {
   const long rows = (long)p.batch.S * p.batch.Q * p.G * p.r;
   long grid = (rows + 7) / 8;
-  // eight CTAs an SM, each warp walking rows: one row a warp and tens of
-  // thousands of short CTAs spend the kernel turning CTAs over (1.32 -> 1.30 ms a step)
+  // eight CTAs an SM, each warp walking rows: with one row a warp, tens of
+  // thousands of short CTAs spend the kernel turning CTAs over
   const long cap = 8L * (num_sms > 0 ? num_sms : 1);
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
