@@ -523,7 +523,7 @@ msa_status_t run_k2q(const msa_cache_t* c, const msa_batch_t* b, const msa_confi
   kp.out = out;
   kp.lse = lse;
   kp.status = at<DeviceStatus>(ws, pl.off_status);
-  if (launch_k2q_build(kp, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (launch_k2q_build(kp, sm_count(), st) != cudaSuccess) return MSA_ERR_CUDA;
   if (launch_k2q_attend(&tk, &tv, kp, sm_count(), st) != cudaSuccess) return MSA_ERR_CUDA;
   if (launch_k2q_combine(kp, sm_count(), st) != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;

@@ -225,7 +225,7 @@ struct InsertParams {
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_insert(const InsertParams& p, int num_sms, cudaStream_t st);
-cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st);    // count, scan, fill
+cudaError_t launch_k2q_build(const K2qParams& p, int num_sms, cudaStream_t st);    // count, scan, fill
 cudaError_t launch_k2q_attend(const CUtensorMap* tk, const CUtensorMap* tv, const K2qParams& p, int num_sms,
                               cudaStream_t st);
 cudaError_t launch_k2q_combine(const K2qParams& p, int num_sms, cudaStream_t st);

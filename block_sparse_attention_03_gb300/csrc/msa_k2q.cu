@@ -5,11 +5,10 @@
 //
 // Count: for every (token, group, slot) whose selected block is b, one more
 // entry in list (sequence, group, b) -- taken token-fastest, so that a warp's
-// lanes mostly share lists and one atomic serves each group of them; the same
-// pass splits each bf16 query row into the e4m3 hi + lo terms the attend's MMA
-// reads.  Scan (one CTA): each
-// list's first entry and first attend item (item_tokens = 128 / r entries an
-// item: one MMA row per (token, head)).  Fill: every entry (token * 32 + slot)
+// lanes mostly share lists and one atomic serves each group of them.  Scan (one
+// CTA): each list's first entry and first attend item (item_tokens = 128 / r
+// entries an item: one MMA row per (token, head)); the same launch's other CTAs
+// split each bf16 query row into the e4m3 hi + lo terms the attend's MMA reads.  Fill: every entry (token * 32 + slot)
 // into its list, in arrival order (the per-entry results do not depend on
 // it).  The attend (msa_k2q_tc.cu) reads each item's K/V tile once and writes
 // one partial (o, m, l, 2^ev) per (token, head, slot); combine merges a
@@ -71,14 +70,20 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
       if (lane == __ffs(peers) - 1) atomicAdd(&p.cnt[key], __popc(peers));
     }
   }
-  if (p.q_fp8) return;
+}
+
+// The bf16 query split, by warps w0, w0 + 1, ... of nw (run by the scan
+// launch's extra CTAs: it needs only the caller's queries, and the scan keeps one
+// SM busy).
+__device__ __forceinline__ void k2q_split_queries(const K2qParams& p, int w0, int nw) {
   // bf16 query rows (token, head), a warp each, lane l holding dims 4l .. 4l+3:
   // q x 2^e with the largest e that keeps the row's amax at most 448 (exact),
   // split into e4m3 hi + lo (together all 8 significant bits of bf16), and
   // the row factor 2^-e x col_const
+  const BatchDev bt = p.batch;
   const int rows = bt.S * bt.Q * p.G * p.r;
-  const int nw = gridDim.x * (blockDim.x >> 5);
-  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += nw) {
+  const int lane = threadIdx.x & 31;
+  for (int row = w0 + (threadIdx.x >> 5); row < rows; row += nw) {
     const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q) + (long)row * 128) + lane);
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
@@ -100,8 +105,13 @@ __global__ void __launch_bounds__(256) k2q_count_kernel(const K2qParams p) {
 }
 
 // One CTA of 1024 threads: thread t owns the contiguous lists [t*L/1024, (t+1)*L/1024).
+// CTA 0 scans; CTAs 1.. split the bf16 query rows meanwhile.
 __global__ void __launch_bounds__(1024) k2q_scan_kernel(const K2qParams p) {
   __shared__ int se[64], si[64];  // the warp totals, then their inclusive scan
+  if (blockIdx.x > 0) {
+    k2q_split_queries(p, (blockIdx.x - 1) * 32, (gridDim.x - 1) * 32);
+    return;
+  }
   const BatchDev bt = p.batch;
   const long L = (long)bt.S * p.G * bt.max_nb;
   const int t = threadIdx.x;
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
 
 }  // namespace
 
-cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st) {
+cudaError_t launch_k2q_build(const K2qParams& p, int num_sms, cudaStream_t st) {
   const long L = (long)p.batch.S * p.G * p.batch.max_nb;
   cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)L * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
@@ -278,7 +288,11 @@ cudaError_t launch_k2q_build(const K2qParams& p, cudaStream_t st) {
   if (grid > 4096) grid = 4096;
   if (grid < 1) grid = 1;
   k2q_count_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
-  k2q_scan_kernel<<<1, 1024, 0, st>>>(p);
+  // CTA 0 scans; with a bf16 query, 4 CTAs an SM more split its rows
+  const long qrows = p.q_fp8 ? 0 : (long)p.batch.S * p.batch.Q * p.G * p.r;
+  long qctas = (qrows + 31) / 32;
+  if (qctas > 4L * num_sms) qctas = 4L * num_sms;
+  k2q_scan_kernel<<<(unsigned)(1 + qctas), 1024, 0, st>>>(p);
   k2q_fill_kernel<<<(unsigned)grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
