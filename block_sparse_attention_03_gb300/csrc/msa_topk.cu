@@ -641,8 +641,9 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   const unsigned rows = (unsigned)(p.batch.S * p.batch.Q * p.G);
-  // rows beyond what 256 threads hold in registers (16 keys each): 1024 threads
-  const bool wide = p.batch.max_nb > kTopkThreads * kKeysPerThreadNarrow;
+  // rows of more than 2,048 blocks: 1024 threads, 8 keys or fewer each (shorter
+  // load and max chains per thread; at 4,096 blocks 1 us less than 256 threads)
+  const bool wide = p.batch.max_nb > 2048;
   const unsigned threads = wide ? 1024u : (unsigned)kTopkThreads;
   const unsigned zrows = (unsigned)((p.nzero + threads - 1) / threads);
   cudaLaunchConfig_t cfg = make_cfg(dim3(rows > zrows ? rows : zrows), dim3(threads), 0, st, pdl, attr);
