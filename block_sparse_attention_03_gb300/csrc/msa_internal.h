@@ -201,7 +201,8 @@ struct K2qParams {
   float q_scale, col_const;
   uint8_t* qsplit;           // bf16 query: [S*Q*G*r][2][128] e4m3 hi, lo terms of q x 2^e (per row)
   float* qrowf;              // [S*Q*G*r] 2^-e x col_const
-  uint16_t* part_o;          // [S*Q][topk][G*r][128] fp16 o / l x 2^-ev of each (token, slot, head)
+  uint16_t* part_o;          // [S*Q][topk][G*r][128] fp16 o / l x 2^-ev of each (token, slot, head);
+                             // 16-byte chunk c of a row is stored at chunk c ^ (head % r)
   float* part_ml;            // [S*Q][topk][G*r][4]: m, l, 2^ev, unused
   void* out;                 // bf16 [S*Q][G*r][128]
   float* lse;

@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const int s = token / bt.Q, i = token % bt.Q;
     const int T = bt.seq_len(s);
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
-    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + ((long)token * p.topk * H + h) * 128 + d8);
+    // dims d8 .. + 7 sit in the row's 16-byte chunk (d8 / 8) ^ (head % r)
+    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + ((long)token * p.topk * H + h) * 128) +
+                        ((lane & 15) ^ (h % p.r));
     uint4 ov[KMAX / 2];
 #pragma unroll
     for (int q = 0; q < KMAX / 2; ++q) {  // slot 2q + half

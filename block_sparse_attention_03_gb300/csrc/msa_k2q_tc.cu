@@ -70,7 +70,8 @@ struct TqLayout {
   static constexpr uint32_t ST = OP + 4 * kTqTile;           // the ring of stages
   static constexpr uint32_t S_K = 0, S_V = kTqTile, S_KS = 2 * kTqTile, S_VS = S_KS + kTqScales;
   // the output rows of an item, staged after MMA 2: 128 / r entries of r rows
-  // of 256 bytes, 16 bytes apart (conflict-free stores)
+  // of 256 bytes, 16 r bytes apart; with the rows' 16-byte chunks swizzled by
+  // head (as in the partials) a warp's stores fall in different banks
   static constexpr uint32_t STAGE = tq_round(S_VS + kTqScales + 2048, 1024);
   static constexpr uint32_t HD = ST + kTqStages * STAGE;     // header slots: entries, then words
   static constexpr uint32_t HSLOT = kTqEnt + kTqHdrW * 4;
@@ -121,14 +122,16 @@ __device__ __forceinline__ float tq_ex2(float x) {
 }
 
 // (a, b) as two e4m3 terms, hi + lo, through f16 (a in the low byte of each):
-// hi = e4m3(f16(x)), lo = e4m3(f16(x) - hi), the difference exact in f16.
+// hi = f16(x) rounded to 3 mantissa bits by an integer add and mask (ties away
+// from zero; exact in e4m3 from 2^-6 up, below which the conversion rounds it
+// once more, to e4m3's subnormal step 2^-9), lo = e4m3(f16(x) - hi), the
+// difference exact in f16.  |x| <= 448, so no half carries into the other.
 __device__ __forceinline__ void split2_e4m3(float a, float b, uint32_t& hi, uint32_t& lo) {
   const uint32_t h2 = pack_f16x2(a, b);
+  const uint32_t t2 = (h2 + 0x00400040u) & 0xff80ff80u;
   uint16_t h8, l8;
-  uint32_t back;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(h2));
-  asm("{ .reg .b16 t; mov.b16 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(back) : "h"(h8));
-  const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(t2));
+  const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&h2), *reinterpret_cast<const __half2*>(&t2));
   asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(*reinterpret_cast<const uint32_t*>(&d)));
   hi = h8;
   lo = l8;
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
     const int terms = p.q_fp8 ? 1 : 2;
     const float qconst = p.q_scale * p.col_const;  // an e4m3 query's row factor
     const int hh = m & (r - 1);                     // this row's head within the group
-    const uint32_t epitch = (uint32_t)r * 256u + 16u;  // staged output rows: bytes per entry
+    const uint32_t epitch = (uint32_t)r * 272u;     // staged output rows: bytes per entry
 
     // every thread of the group waits; the group agrees on the outcome
     auto gwait = [&](uint64_t* bar, uint32_t par, int where) -> bool {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
           w.y = pack_f16x2(v[8 * c + 2] * inv, v[8 * c + 3] * inv);
           w.z = pack_f16x2(v[8 * c + 4] * inv, v[8 * c + 5] * inv);
           w.w = pack_f16x2(v[8 * c + 6] * inv, v[8 * c + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + 64 * h + 16 * c) = w;
+          *reinterpret_cast<uint4*>(orow + 16 * ((4 * h + c) ^ hh)) = w;  // the partials' swizzle
         }
       }
       // the rows written here are read next by the bulk copies (and later
