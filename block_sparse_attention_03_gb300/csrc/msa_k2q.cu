@@ -219,9 +219,9 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
     const int s = token / bt.Q, i = token % bt.Q;
     const int T = bt.seq_len(s);
     const int last = (T < bt.Q || T > bt.max_nb * kBlock) ? -1 : min(bt.max_nb - 1, (T - bt.Q + i) / kBlock);
-    // dims d8 .. + 7 sit in the row's 16-byte chunk (d8 / 8) ^ (head % r)
-    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + ((long)token * p.topk * H + h) * 128) +
-                        ((lane & 15) ^ (h % p.r));
+    // the lane's 16-byte chunk of every slot's row holds dims 8 ((lane % 16) ^
+    // (head % r)) .. + 7 (the attend's swizzle, the same for all the row's slots)
+    const uint4* orow = reinterpret_cast<const uint4*>(p.part_o + ((long)token * p.topk * H + h) * 128 + d8);
     uint4 ov[KMAX / 2];
 #pragma unroll
     for (int q = 0; q < KMAX / 2; ++q) {  // slot 2q + half
@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
       pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
       pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
       pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (long)row * 128 + d8) = pk;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (long)row * 128 + 8 * ((lane & 15) ^ (h % p.r))) =
+          pk;
     }
     if (lane == 0 && p.lse) p.lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
   }
