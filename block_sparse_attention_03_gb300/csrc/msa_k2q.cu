@@ -201,8 +201,9 @@ __device__ __forceinline__ float k2q_ex2(float x) {
 // One warp per (token, head): the token's selected slots merged by
 // log-sum-exp in base 2 (m and l come that way).  Every load of the row is
 // issued at once: lane k < topk takes slot k's (m, l, 2^ev), and the two
-// half-warps take the even and the odd slots' o / l rows, lane l holding dims
-// 8 (l % 16) .. + 7 with one 16-byte load a slot (32 slots at most).
+// half-warps take the even and the odd slots' o / l rows, lane l holding the
+// row's 16-byte chunk l % 16 (dims 8 ((l % 16) ^ (head % r)) .. + 7, the
+// attend's swizzle) with one load a slot (32 slots at most).
 template <int KMAX>
 __global__ void __launch_bounds__(256) k2q_combine_kernel(const K2qParams p) {
   const BatchDev bt = p.batch;
