@@ -79,6 +79,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int ma
   return false;
 }
 
+// The same wait for kernels whose warps wait long and many at a time (the
+// prefill indexer and attend): each try_wait may suspend the thread for up to
+// kWaitSuspendNs, woken by the phase's completion, instead of re-testing
+// (the re-tests of many waiting warps kept the shared-memory pipe busy);
+// max_tries of them take at most max_tries x 10 us (2 s by default).  The
+// decode kernels' short, latency-critical waits keep the plain test.
+constexpr uint32_t kWaitSuspendNs = 10000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int max_tries = 200000) {
+  const uint32_t a = smem_u32(bar);
+#pragma unroll 1
+  for (int i = 0; i < max_tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(a), "r"(parity), "n"(kWaitSuspendNs)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // Warp-uniform wait: every lane polls, the warp agrees on the outcome.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int max_tries = 4000000) {
   const uint32_t a = smem_u32(bar);

@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
           if (jh < nj) {  // header jh
             const int hs = jh % kTqHdrs;
             if (jh >= kTqHdrs && (*reinterpret_cast<volatile int*>(dead) ||
-                                  !mbar_wait(&hempty[hs], (uint32_t)(((jh / kTqHdrs) - 1) & 1)))) {
+                                  !mbar_wait_sleep(&hempty[hs], (uint32_t)(((jh / kTqHdrs) - 1) & 1)))) {
               fail(24);
             } else {
               uint8_t* hb = base + LY::HD + (size_t)hs * LY::HSLOT;
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
           if (ok && jk >= 0) {  // tiles of item jk
             const int st = jk % kTqStages;
             if (jk >= kTqStages && (*reinterpret_cast<volatile int*>(dead) ||
-                                    !mbar_wait(&kvempty[st], (uint32_t)(((jk / kTqStages) - 1) & 1)))) {
+                                    !mbar_wait_sleep(&kvempty[st], (uint32_t)(((jk / kTqStages) - 1) & 1)))) {
               fail(20);
             } else {
               const int tile = reinterpret_cast<const int32_t*>(base + LY::HD + (size_t)(jk % kTqHdrs) * LY::HSLOT +
@@ -288,11 +288,11 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
     if (lane == 0 && !ok) {
       for (int i = 0; i < kTqHdrs && i < issued_h; ++i) {
         const int jj = issued_h - 1 - i;
-        mbar_wait(&hfull[jj % kTqHdrs], (uint32_t)((jj / kTqHdrs) & 1), 2000);
+        mbar_wait_sleep(&hfull[jj % kTqHdrs], (uint32_t)((jj / kTqHdrs) & 1), 2000);
       }
       for (int i = 0; i < kTqStages && i < issued_k; ++i) {
         const int jj = issued_k - 1 - i;
-        mbar_wait(&kvfull[jj % kTqStages], (uint32_t)((jj / kTqStages) & 1), 2000);
+        mbar_wait_sleep(&kvfull[jj % kTqStages], (uint32_t)((jj / kTqStages) & 1), 2000);
       }
     }
   } else {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
 
     // every thread of the group waits; the group agrees on the outcome
     auto gwait = [&](uint64_t* bar, uint32_t par, int where) -> bool {
-      const bool ok = !*reinterpret_cast<volatile int*>(dead) && mbar_wait(bar, par);
+      const bool ok = !*reinterpret_cast<volatile int*>(dead) && mbar_wait_sleep(bar, par);
       const bool bad = named_bar_or(bar_id, 128, !ok);
       if (bad && leader && !*reinterpret_cast<volatile int*>(dead)) {
         *reinterpret_cast<volatile int*>(dead) = 1;
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(kTqThreads, 1) k2q_tc_kernel(const __grid_cons
     // every MMA this leader issued has completed before TMEM is freed
     if (leader) {
       mma_commit(&done[grp]);
-      mbar_wait(&done[grp], 0, 200000);
+      mbar_wait_sleep(&done[grp], 0, 200000);
     }
   }
   tc_fence_before();

@@ -145,7 +145,7 @@ __device__ __forceinline__ void pi_advance(const BatchDev& bt, int tiles, UnitCu
 
 __device__ __forceinline__ bool pi_wait(uint64_t* bar, uint32_t parity, int* dead, DeviceStatus* st, int where) {
   if (*reinterpret_cast<volatile int*>(dead)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait_sleep(bar, parity)) return true;
   *reinterpret_cast<volatile int*>(dead) = 1;
   raise_flag(st, FLAG_TIMEOUT, where);
   return false;
@@ -270,11 +270,11 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
     if (lane == 0) {
       for (int i = 0; i < NSTG && i < issued; ++i) {
         const int jj = issued - 1 - i;
-        mbar_wait(&kfull[jj % NSTG], (uint32_t)((jj / NSTG) & 1), 2000);
+        mbar_wait_sleep(&kfull[jj % NSTG], (uint32_t)((jj / NSTG) & 1), 2000);
       }
       for (int i = 0; i < kPiSStages && i < issued; ++i) {
         const int jj = issued - 1 - i;
-        mbar_wait(&sfull[jj % kPiSStages], (uint32_t)((jj / kPiSStages) & 1), 2000);
+        mbar_wait_sleep(&sfull[jj % kPiSStages], (uint32_t)((jj / kPiSStages) & 1), 2000);
       }
     }
   } else if (warp == 1) {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kPiThreads, 1) pindexer_kernel(const __grid_co
         if (j + 1 == nunits || c.qt != cur_tile || c.s != cur_s) mma_commit(aempty);  // the query tile is free
       }
       mma_commit(done);
-      mbar_wait(done, 0, 200000);
+      mbar_wait_sleep(done, 0, 200000);
     }
   } else {
     // ---------------- query tiles + epilogue (thread = accumulator row)
