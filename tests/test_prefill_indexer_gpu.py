@@ -196,6 +196,7 @@ def test_prefill_selection_equals_block_topk(mode, zero_idx, init, local, k, ove
     (dict(seq_lens=(2500, 1300), q_per_seq=16, topk=32), None),             # 32 slots a token
     (dict(seq_lens=(3000,), q_per_seq=20), dict(init_blocks=1, local_blocks=2)),
     (dict(seq_lens=(2100,), q_per_seq=40, num_q_heads=32), None),           # 8 q heads a group: 16 tokens an item
+    (dict(seq_lens=(2900,), q_per_seq=24, num_q_heads=32, topk=32), None),  # 8 heads a group and 32 slots a token
     (dict(seq_lens=(1900, 700), q_per_seq=24, num_q_heads=8, q_dtype="fp8"), None),  # 2 a group, e4m3 query
     (dict(seq_lens=(6000,), q_per_seq=300), None),                           # lists of several items
 ])
